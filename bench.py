@@ -1,0 +1,382 @@
+#!/usr/bin/env python3
+"""Benchmark of the QK-Normed MLA decode path on GB300.
+
+One step = one pass of the whole path over one batch: qkmla_absorb_query,
+qkmla_append of the step's new latents, qkmla_decode (with its split-KV
+combine).  Inputs are synthetic (seeded), resident in HBM before timing.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl ours|reference]
+
+Under torchrun each rank runs its own copy of the workload (different seeds):
+the path shards by sequence with no data-path collective (weak scaling).
+Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20          # > 129 MB L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", type=int, default=1, help="index into workloads.WORKLOADS")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-plain", action="store_true", help="skip the plain-MLA comparator timing")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                    "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))}, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic(w: W.Workload, lens: np.ndarray, plain: bool = False):
+    """Algorithmic bytes and MMA flops of one decode call.
+
+    Bytes: every cached token's row (latent + RoPE key) once, its G alpha^k
+    scalars (not in plain mode), the query side (q~ in the cache dtype, alpha^q,
+    q_rope fp32) and the fp32 output + lse.  Flops: for every (query, visible
+    token, head) 2*(d_c + d_r) for the logit and 2*d_c for the output.
+    """
+    cb = 4 if w.cache_dtype == "f32" else 2
+    tokens = int(lens.sum())
+    kv_bytes = tokens * (w.d_c + w.d_r) * cb + (0 if plain else tokens * w.G * 4)
+    rows = w.B * w.s_q * w.H
+    q_bytes = rows * (w.d_c * cb + 4 + w.d_r * 4)
+    o_bytes = rows * (w.d_c * 4 + 4)
+    visible = sum(int(L) - w.s_q + i + 1 for L in lens for i in range(w.s_q))
+    flops = visible * w.H * 2 * (2 * w.d_c + w.d_r)
+    return kv_bytes + q_bytes + o_bytes, flops, kv_bytes
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_from_profiles(kernel_sig: str):
+    """dram bytes per launch recorded by an ncu capture of the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    for ln in open(p):
+        f = dict(kv.split("=", 1) for kv in ln.split() if "=" in kv)
+        if f.get("sig") == kernel_sig and "bytes_per_launch" in f:
+            return float(f["bytes_per_launch"])
+    return None
+
+
+def kernel_signature():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "qk_normed_latent_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (baseline; oracle as it stands)
+# ----------------------------------------------------------------------------
+def cpu_oracle_rate(w: W.Workload, target_s: float):
+    """Time the oracle's whole path (absorb, append of the sequence, explicit
+    decode) on whole sequences until about target_s seconds of work.  Returns
+    (tokens/s, sample description, threads)."""
+    import oracle as O
+    wk, gq, gk, grq, grk = W.weights(w)
+    q, qr = W.queries(w)
+    lens = W.seq_lens(w)
+    order = list(np.argsort(lens))            # shortest first: bounded sample
+    t_total, done, toks = 0.0, [], 0
+    for b in order:
+        b = int(b)
+        c, r = W.sequence(w, b)
+        t0 = time.perf_counter()
+        ch, rh, ak = O.append_tokens(c, r, wk, grk, w.eps, w.cache_dtype)
+        O.absorb_query(q[b].reshape(w.s_q, w.H, w.d_h), gq, gk, wk, w.eps)
+        O.decode_explicit(q[b:b + 1], qr[b:b + 1], gq, gk, grq, wk, [(ch, rh)], w.s_q, w.scale, w.eps)
+        t_total += time.perf_counter() - t0
+        done.append(b)
+        toks += w.s_q
+        if t_total >= target_s:
+            break
+    ctx = int(sum(int(lens[b]) for b in done))
+    sample = (f"{len(done)} of {w.B} sequences ({ctx} cached tokens), whole path: oracle append of the "
+              f"sequence (alpha^k over all groups), absorb, explicit decode with materialised keys")
+    return toks / t_total, sample, t_total
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w0 = W.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        rate, sample, secs = 0.0, "", 0.0
+        step_rates = []
+        for _ in range(args.warmup):
+            cpu_oracle_rate(W.small(w0, 1, (min(256, int(W.seq_lens(w0).min())),)), 0.0)
+        for _ in range(max(1, args.steps)):
+            r_, sample, secs = cpu_oracle_rate(w0, args.cpu_seconds / max(1, args.steps))
+            step_rates.append(r_)
+        rate = statistics.median(step_rates)
+        line = {"impl": "reference", "metric": "decode tokens/s", "value": rate, "unit": "tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1000.0 * w0.B * w0.s_q / rate, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w0.name, "B": w0.B, "s_q": w0.s_q, "H": w0.H, "G": w0.G, "d_c": w0.d_c,
+                           "d_h": w0.d_h, "d_r": w0.d_r, "cache": w0.cache_dtype},
+                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                                 "sample": sample + " per step"},
+                "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = w0.with_(seed=w0.seed + 7919 * rank) if rank else w0
+
+    from qk_normed_latent_gb300 import build as B
+    B.build()
+    import qk_normed_latent_gb300 as Q
+    from qk_normed_latent_gb300.pipeline import DeviceState
+
+    st = DeviceState(w)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    lens = W.seq_lens(w)
+    bytes_alg, flops_alg, _ = algorithmic(w, lens)
+    pk, pk_kind = peaks()
+    for _ in range(max(3, args.warmup)):
+        st.step()
+    torch.cuda.synchronize()
+    if Q.get_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+    kernel = Q.decode_kernel_name(st.args)
+    launches_per_step = 1 + (1 if st.c_new is not None else 0) + 1 + (1 if Q.decode_workspace_size(st.args) else 0)
+
+    def timed_steps(state, K):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for k in range(K):
+            flush.fill_(k & 0xFF)                       # evict the cache from L2 between steps
+            e0, e1, e2 = ev[k]
+            e0.record(stream)
+            state.absorb()
+            state.append_step()
+            e1.record(stream)
+            Q.decode_raw(state.args)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        step_ms = [a.elapsed_time(c) for a, _, c in ev]
+        dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+        return step_ms, dec_ms
+
+    clk = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk.start()
+    time.sleep(0.3)
+    step_ms, dec_ms = timed_steps(st, args.steps)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = clk.stop()
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if Q.get_device_status() != 0:
+        raise RuntimeError("device status error in the timed region")
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = w.B * w.s_q
+    value = tokens_per_step * world / (total_ms / 1e3 / args.steps) / 1.0
+    dec_avg = statistics.mean(dec_ms)
+
+    # roofline of the dominant kernel (the decode call: decode kernel + combine)
+    t_hbm = bytes_alg / (pk["hbm_gbs"] * 1e9)
+    t_mma = flops_alg / (pk["bf16_tflops"] * 1e12)
+    if t_hbm >= t_mma:
+        roof = {"bound": "hbm", "achieved": bytes_alg / (dec_avg * 1e-3) / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops_alg / (dec_avg * 1e-3) / 1e12, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic_from_profiles(kernel_signature() + ":" + w.name)
+    roof["peak_source"] = f"{pk_kind} (MEASURED_PEAKS.json)" if pk_kind == "measured" else "fallback (6.8 TB/s, 1.9 PF/s)"
+    roof["kernel"] = f"qkmla_decode[{kernel}]"
+    roof["algorithmic_bytes_per_launch"] = bytes_alg
+    roof["algorithmic_flops_per_launch"] = flops_alg
+    roof["roofline_us"] = max(t_hbm, t_mma) * 1e6
+
+    # plain-MLA comparator: same kernels with the alpha scaling off
+    plain = None
+    if not args.no_plain:
+        sp = DeviceState(w, plain=True)
+        for _ in range(3):
+            sp.step()
+        torch.cuda.synchronize()
+        p_step, p_dec = timed_steps(sp, min(args.steps, 100))
+        q_step, q_dec = timed_steps(st, min(args.steps, 100))
+        plain = {"decode_ms": statistics.median(p_dec), "qknorm_decode_ms": statistics.median(q_dec),
+                 "overhead_pct": 100.0 * (statistics.median(q_dec) / statistics.median(p_dec) - 1.0),
+                 "step_overhead_pct": 100.0 * (statistics.median(q_step) / statistics.median(p_step) - 1.0)}
+        del sp
+
+    # end to end through the public API with host buffers: H2D of the step's inputs,
+    # the three calls, D2H of o and lse, all inside the timed region
+    h_q = torch.from_numpy(st.q_host.reshape(w.rows, w.H, w.d_h)).pin_memory()
+    h_qr = torch.from_numpy(st.qr_host).pin_memory()
+    h_in = [(h_q, st.q), (h_qr, st.q_rope)]
+    if st.c_new is not None:
+        h_in += [(st.c_new.cpu().pin_memory(), st.c_new), (st.r_new.cpu().pin_memory(), st.r_new),
+                 (st.slots_new.cpu().pin_memory(), st.slots_new)]
+    h_o = torch.empty(st.o.shape, dtype=st.o.dtype).pin_memory()
+    h_l = torch.empty(st.lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for h, _ in h_in)
+    d2h = h_o.numel() * h_o.element_size() + h_l.numel() * 4
+    K2 = min(args.steps, 100)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
+    for k in range(K2):
+        flush.fill_(k & 0xFF)
+        ev[k][0].record(stream)
+        for h, d in h_in:
+            d.copy_(h, non_blocking=True)
+        st.step()
+        h_o.copy_(st.o, non_blocking=True)
+        h_l.copy_(st.lse, non_blocking=True)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in ev) / K2
+    e2e = {"value": tokens_per_step * world / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, sample, secs = cpu_oracle_rate(w, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample,
+               "seconds": secs}
+
+    if rank == 0:
+        line = {
+            "metric": "decode tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.cache_dtype,
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "s_q": w.s_q, "H": w.H, "G": w.G, "d_c": w.d_c,
+                       "d_h": w.d_h, "d_r": w.d_r, "cache": w.cache_dtype,
+                       "context_tokens": int(lens.sum()), "n_append_per_seq": w.n_append,
+                       "page_size": w.page_size, "parallelism": f"dp{world} (replicas, no collective)",
+                       "l2": "flushed before every step (256 MiB fill outside the timed intervals)"},
+            "decode_ms": dec_avg,
+            "kv_gbs": bytes_alg / (dec_avg * 1e-3) / 1e9,
+            "roofline": roof,
+            "plain_mla": plain,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -48,7 +48,7 @@ import numpy as np
 
 __all__ = [
     "bf16_rne", "cache_cast", "inv_rms", "group_of_head",
-    "absorb_query", "append_tokens", "full_keys",
+    "absorb_query", "append_tokens", "rope_key", "full_keys",
     "decode_explicit", "decode_absorbed", "combine_partials",
     "valid_length", "cache_write", "cache_gather",
 ]
@@ -145,15 +145,22 @@ def append_tokens(c_new, r_new, w_k, gamma_rk, eps: float, cache_dtype: str, pla
     r = np.asarray(r_new, dtype=np.float64)
     if plain:
         ak = np.ones((N, G))
-        r_hat = cache_cast(np.asarray(r_new, np.float32), cache_dtype)
-        return c_hat, r_hat, ak
+        return c_hat, rope_key(r_new, gamma_rk, eps, cache_dtype, plain=True), ak
     ak = np.empty((N, G))
     for g in range(G):
         ak[:, g] = inv_rms(c_hat @ w[g], eps)
+    return c_hat, rope_key(r_new, gamma_rk, eps, cache_dtype), ak
+
+
+def rope_key(r_new, gamma_rk, eps: float, cache_dtype: str, plain: bool = False) -> np.ndarray:
+    """Stored RoPE key ([BLK]): r (.) gamma_rk / S(r), rounded to the cache dtype
+    (plain mode: the rounded raw key)."""
+    if plain:
+        return cache_cast(np.asarray(r_new, np.float32), cache_dtype)
+    r = np.asarray(r_new, dtype=np.float64)
     gr = np.ones(r.shape[1]) if gamma_rk is None else np.asarray(gamma_rk, np.float64)
     beta = inv_rms(r, eps)
-    r_hat = cache_cast((r * gr * beta[:, None]).astype(np.float32), cache_dtype)
-    return c_hat, r_hat, ak
+    return cache_cast((r * gr * beta[:, None]).astype(np.float32), cache_dtype)
 
 
 def full_keys(c_hat, w_k) -> np.ndarray:

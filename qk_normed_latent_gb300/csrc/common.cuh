@@ -1,0 +1,82 @@
+// Shared device helpers of the QK-Normed MLA decode library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/qkmla.h"
+
+namespace qkmla {
+
+// Record the first device-side error in the per-device status word `st`
+// (read and cleared by qkmla_get_device_status()).
+__device__ __forceinline__ void report(int* st, int code) {
+    if (st) atomicCAS(st, 0, code);
+}
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float load(const float* p) { return *p; }
+    static __device__ __forceinline__ float cast(float x) { return x; }
+    static __device__ __forceinline__ void store(float* p, float x) { *p = x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+    static __device__ __forceinline__ float cast(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Physical slot of token t of sequence b (see the cache convention in qkmla.h).
+// Returns -1 (and records a bounds error) for a page id outside [0, num_pages).
+__device__ __forceinline__ int64_t slot_of(const int32_t* page_table, int b, int t, int page_size,
+                                           int max_pages, int64_t num_pages, int* st) {
+    const int p = t / page_size;
+    const int64_t page = page_table ? (int64_t)page_table[(int64_t)b * max_pages + p]
+                                    : (int64_t)b * max_pages + p;
+    if (page < 0 || page >= num_pages) {
+        report(st, QKMLA_ERR_DEVICE_BOUNDS);
+        return -1;
+    }
+    return page * page_size + (t % page_size);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+}  // namespace qkmla
+
+// Launch-side helpers (host).
+namespace qkmla {
+int launch_absorb(const float* q, const float* gq, const float* gk, const float* wk, int rows, int H,
+                  int G, int d_h, int d_c, float eps, bool plain, void* qt, int qt_dtype, float* aq,
+                  cudaStream_t s);
+int launch_append(const float* c_new, const float* r_new, const float* wk, const float* grk,
+                  const int64_t* slots, int N, int G, int d_c, int d_h, int d_r, float eps, bool plain,
+                  void* kv, int cache_dtype, float* ak, int64_t num_slots, cudaStream_t s);
+
+struct DecodePlan {
+    int kernel;            // 0 = simt, 1 = tcgen05
+    int num_splits;        // simt: splits per sequence
+    int parts;             // number of partial (o, lse) records in the workspace
+    size_t ws_bytes;
+};
+int plan_decode(const qkmla_decode_args* a, DecodePlan* plan);
+int launch_decode_simt(const qkmla_decode_args* a, const DecodePlan& plan, cudaStream_t s);
+int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStream_t s);
+int launch_combine(const float* o_part, const float* lse_part, int rows, int nsplit, int d_c, void* o,
+                   int o_dtype, float* lse, cudaStream_t s);
+int device_sm_count();
+int* device_status_ptr();   // this device's status word (lazily resolved), or nullptr
+}  // namespace qkmla

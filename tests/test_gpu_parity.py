@@ -1,0 +1,257 @@
+"""GPU parity: every call of the CUDA path against the fp64 CPU oracle on the
+same seeded inputs.
+
+Tolerances (fixed for this method): bf16 cache with fp32 accumulation --
+max-abs <= 2e-2 and relative L2 <= 5e-3 on o and lse; fp32 cache -- relative
+L2 <= 1e-5 and |diff| <= 1e-5 * max(1, |ref|) element-wise.  Cache writes are
+compared bit for bit where the operation is a pure cast.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import oracle.run as OR
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def Q():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from qk_normed_latent_gb300 import build as B
+    B.build()
+    import qk_normed_latent_gb300 as Q
+    return Q
+
+
+def check_close(got, ref, kind, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    d = np.abs(got - ref)
+    rel_l2 = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    if kind == "f32":
+        assert rel_l2 <= 1e-5, f"{what}: rel-L2 {rel_l2:.3e}"
+        worst = np.max(d / np.maximum(1.0, np.abs(ref)))
+        assert worst <= 1e-5, f"{what}: elementwise {worst:.3e}"
+    else:
+        assert d.max() <= 2e-2, f"{what}: max-abs {d.max():.3e}"
+        assert rel_l2 <= 5e-3, f"{what}: rel-L2 {rel_l2:.3e}"
+    return float(d.max()), float(rel_l2)
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy()
+
+
+# ---------------------------------------------------------------------------
+# qkmla_absorb_query
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("widx", [0, 1, 2, 4])
+@pytest.mark.parametrize("qt", ["f32", "bf16"])
+@pytest.mark.parametrize("plain", [False, True])
+def test_absorb_matches_oracle(Q, widx, qt, plain):
+    w = W.WORKLOADS[widx]
+    wk, gq, gk, _, _ = W.weights(w)
+    q, _ = W.queries(w)
+    q = q.reshape(w.rows, w.H, w.d_h)
+    d = "cuda"
+    dt = torch.float32 if qt == "f32" else torch.bfloat16
+    qt_out = torch.empty((w.rows, w.H, w.d_c), dtype=dt, device=d)
+    aq_out = torch.empty((w.rows, w.H), dtype=torch.float32, device=d)
+    Q.absorb_query(torch.from_numpy(q).to(d), torch.from_numpy(gq).to(d), torch.from_numpy(gk).to(d),
+                   torch.from_numpy(wk).to(d), w.eps, qt_out, aq_out, plain=plain)
+    torch.cuda.synchronize()
+    ref_qt, ref_aq = O.absorb_query(q, gq, gk, wk, w.eps, plain=plain)
+    np.testing.assert_allclose(_np(aq_out), ref_aq, rtol=2e-6)
+    g = _np(qt_out)
+    if qt == "f32":
+        assert np.max(np.abs(g - ref_qt)) <= 1e-5 * max(1.0, np.abs(ref_qt).max())
+    else:
+        # one bf16 rounding of an fp32 value: within one bf16 ulp of the exact value
+        ulp = np.maximum(np.abs(ref_qt), 1e-30) * 2.0 ** -7
+        assert np.all(np.abs(g - ref_qt) <= ulp + 1e-6)
+
+
+# ---------------------------------------------------------------------------
+# qkmla_append: layout and values
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cache", ["f32", "bf16"])
+@pytest.mark.parametrize("plain", [False, True])
+@pytest.mark.parametrize("widx", [1, 2])
+def test_append_matches_oracle_bit_exact_layout(Q, cache, plain, widx):
+    w = W.WORKLOADS[widx].with_(cache_dtype=cache)
+    wk, _, _, _, grk = W.weights(w)
+    grk = (1 + 0.1 * np.random.default_rng(5).standard_normal(w.d_r)).astype(np.float32)  # non-trivial gamma
+    c, r = W.sequence(W.small(w, 1, (301,)), 0)
+    num_slots = 1024
+    rng = np.random.default_rng(7)
+    slots = rng.choice(num_slots, size=301, replace=False).astype(np.int64)
+    slots[::17] = -1                                          # skipped tokens
+    d = "cuda"
+    cdt = torch.float32 if cache == "f32" else torch.bfloat16
+    kv = torch.empty((num_slots, w.d_c + w.d_r), dtype=cdt, device=d)
+    ak = torch.empty((num_slots, w.G), dtype=torch.float32, device=d)
+    from qk_normed_latent_gb300.pipeline import sentinel_fill
+    sentinel_fill(kv)
+    sentinel_fill(ak)
+    kv0 = kv.clone()
+    ak0 = ak.clone()
+    Q.append(torch.from_numpy(c).to(d), torch.from_numpy(r).to(d), torch.from_numpy(wk).to(d),
+             torch.from_numpy(grk).to(d), torch.from_numpy(slots).to(d), kv, ak, w.eps, plain=plain)
+    assert Q.get_device_status() == 0
+    ch, rh, a = O.append_tokens(c, r, wk, grk, w.eps, cache, plain=plain)
+    ok = slots >= 0
+    kvh = kv.cpu()
+    # latent: a pure cast -> bit-exact against the oracle's RNE cast
+    lat = kvh[torch.from_numpy(slots[ok]), : w.d_c].float().numpy()
+    np.testing.assert_array_equal(lat.astype(np.float64), ch[ok])
+    # RoPE key: one rounding of an fp32 product -> within one cache ulp
+    rope = kvh[torch.from_numpy(slots[ok]), w.d_c:].float().numpy()
+    ulp = 2.0 ** (-7 if cache == "bf16" else -23)
+    assert np.all(np.abs(rope - rh[ok]) <= ulp * np.abs(rh[ok]) + 1e-30)
+    # alpha^k: fp32 GEMM + reduction vs fp64
+    np.testing.assert_allclose(ak.cpu().numpy()[slots[ok]], a[ok], rtol=1e-5)
+    # untouched slots keep their sentinel bits
+    untouched = np.setdiff1d(np.arange(num_slots), slots[ok])
+    iv = torch.int16 if cache == "bf16" else torch.int32
+    assert torch.equal(kvh[untouched].view(iv), kv0.cpu()[untouched].view(iv))
+    assert torch.equal(ak.cpu()[untouched].view(torch.int32), ak0.cpu()[untouched].view(torch.int32))
+
+
+def test_append_out_of_range_slot_is_reported(Q):
+    w = W.WORKLOADS[1]
+    wk = torch.from_numpy(W.weights(w)[0]).cuda()
+    kv = torch.zeros((128, w.d_c + w.d_r), dtype=torch.bfloat16, device="cuda")
+    ak = torch.zeros((128, w.G), dtype=torch.float32, device="cuda")
+    c = torch.randn(2, w.d_c, device="cuda")
+    r = torch.randn(2, w.d_r, device="cuda")
+    slots = torch.tensor([5, 128], dtype=torch.int64, device="cuda")
+    Q.append(c, r, wk, None, slots, kv, ak, w.eps)
+    assert Q.get_device_status() == Q.ERR_DEVICE_BOUNDS
+    assert Q.get_device_status() == 0            # cleared by the read
+    assert torch.count_nonzero(kv[5]) > 0
+
+
+# ---------------------------------------------------------------------------
+# qkmla_decode end to end (absorb -> append -> decode) against the explicit definition
+# ---------------------------------------------------------------------------
+CASES = {
+    "tiny_fp32": (0, None),
+    "small_bf16_full": (1, None),
+    "dsv3_B4_T4096": (2, dict(B=4, lens=(4096, 4096, 4096, 4096))),
+    "dsv3_ragged": (2, dict(B=6, lens=(1, 63, 64, 65, 129, 3001))),
+    "long_ctx_B1_T20000": (3, dict(B=1, lens=(20011,))),
+    "mixed_sq2_ragged": (4, dict(B=6, lens=(2, 64, 65, 130, 777, 5000))),
+}
+
+
+def _workload(name):
+    widx, red = CASES[name]
+    w = W.WORKLOADS[widx]
+    if red:
+        w = W.small(w, red["B"], red["lens"])
+    return w
+
+
+@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("plain", [False, True])
+def test_decode_end_to_end_matches_oracle(Q, name, plain):
+    from qk_normed_latent_gb300.pipeline import DeviceState
+    w = _workload(name)
+    st = DeviceState(w, plain=plain)
+    st.step()
+    assert Q.get_device_status() == 0
+    o_ref, lse_ref = OR.reference(w, plain=plain)
+    check_close(_np(st.o), o_ref, w.cache_dtype, f"{name} o")
+    check_close(_np(st.lse), lse_ref, w.cache_dtype, f"{name} lse")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 33])
+@pytest.mark.parametrize("simt", [False, True])
+def test_decode_split_counts_agree(Q, splits, simt):
+    from qk_normed_latent_gb300.pipeline import DeviceState
+    w = _workload("dsv3_ragged")
+    st = DeviceState(w)
+    st.absorb()
+    st.append_step()
+    st.decode(num_splits=0, force_simt=simt)
+    o_auto, l_auto = _np(st.o).copy(), _np(st.lse).copy()
+    st.decode(num_splits=splits, force_simt=simt)
+    assert Q.get_device_status() == 0
+    o_ref, lse_ref = OR.reference(w)
+    check_close(_np(st.o), o_ref, "bf16", f"splits={splits} o")
+    check_close(_np(st.lse), lse_ref, "bf16", f"splits={splits} lse")
+    # different split counts only change fp32 rounding
+    assert np.max(np.abs(_np(st.o) - o_auto)) <= 1e-3
+    assert np.max(np.abs(_np(st.lse) - l_auto)) <= 1e-3
+
+
+def test_decode_bad_page_id_is_reported_not_trapped(Q):
+    from qk_normed_latent_gb300.pipeline import DeviceState
+    w = _workload("dsv3_ragged")
+    st = DeviceState(w)
+    st.step()
+    assert Q.get_device_status() == 0
+    bad = st.page_table.clone()
+    bad[5, 3] = 10 ** 6                     # outside [0, num_pages)
+    st.page_table = bad
+    st.args = None
+    st.decode(force_simt=True)
+    assert Q.get_device_status() == Q.ERR_DEVICE_BOUNDS
+    st.decode()
+    assert Q.get_device_status() == Q.ERR_DEVICE_BOUNDS
+    # a length beyond the page table is reported too
+    st.page_table = st.page_table.clone()
+    st.page_table[5, 3] = 0
+    st.seq_lens[1] = st.max_pages * st.page_size + 1
+    st.decode()
+    assert Q.get_device_status() == Q.ERR_DEVICE_BOUNDS
+
+
+def test_decode_workspace_too_small_is_rejected(Q):
+    from qk_normed_latent_gb300.pipeline import DeviceState
+    w = _workload("dsv3_B4_T4096")
+    st = DeviceState(w)
+    st.absorb()
+    a = st.decode_args(num_splits=4)
+    need = Q.decode_workspace_size(a)
+    assert need > 0
+    a.workspace_bytes = need - 1
+    with pytest.raises(Q.QkmlaError) as e:
+        Q.decode_raw(a)
+    assert e.value.code == Q.ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, in the bench's launch configuration: sampled sequences
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("widx,picks,heads", [
+    (1, (0, 7, 15), None),
+    (2, (0, 33, 63), None),
+    (3, (2,), tuple(range(16, 32))),
+    (4, "spread", tuple(range(0, 16)) + tuple(range(112, 128))),
+])
+def test_full_size_sampled_rows(Q, widx, picks, heads):
+    from qk_normed_latent_gb300.pipeline import DeviceState
+    w = W.WORKLOADS[widx]
+    st = DeviceState(w)
+    st.step()
+    assert Q.get_device_status() == 0
+    if picks == "spread":
+        order = np.argsort(W.seq_lens(w))
+        picks = (int(order[0]), int(order[len(order) // 2]), int(order[-1]))
+    o_ref, lse_ref = OR.reference(w, seqs=picks, heads=heads)
+    o = _np(st.o)[list(picks)]
+    lse = _np(st.lse)[list(picks)]
+    hsel = slice(None) if heads is None else list(heads)
+    check_close(o[:, :, hsel], o_ref[:, :, hsel], w.cache_dtype, f"w{widx} o")
+    check_close(lse[:, :, hsel], lse_ref[:, :, hsel], w.cache_dtype, f"w{widx} lse")
+    # every output row is finite and lse is bounded by the normalised-logit bound
+    assert np.all(np.isfinite(_np(st.o))) and np.all(np.isfinite(_np(st.lse)))
