@@ -1,6 +1,802 @@
-// Tensor-core (tcgen05 / TMEM / TMA) decode kernel -- placeholder until built.
+// Tensor-core decode kernel for a bf16 latent cache (tcgen05 + TMEM + TMA).
+//
+// Source: "QK-Normed MLA: QK normalization without full key caching", Technical
+// Summary, Methodology -- decode-logit equation l = (q~ . c_t) alpha^q alpha^k_{t,g(h)}
+// with the scalars applied as a row/column scaling of the logit tile before the
+// softmax; "Blockwise Normalization" (separately normalised RoPE logit); the
+// Significance section's note that speed depends on fusing the scalar factors
+// into the attention path.  Values are the latents (latent decode path).
+//
+// Work decomposition.  A CTA owns 64 query rows (heads of one query token) of
+// one sequence and a contiguous range of 64-token tiles.  Per tile:
+//   S_c = Q~ C^T   (M=64 rows, N=64 tokens, K=d_c)   tcgen05, fp32 in TMEM
+//   S_r = Q^r K^rT (M=64,      N=64,        K=d_r)   tcgen05, fp32 in TMEM
+//   l   = scale*(alpha^q_row * alpha^k_{t,g(row)} * S_c + S_r)      (fused, fp32)
+//   P   = exp2(l*log2e - m_row), stored bf16 into the tile's RoPE slot
+//   O^T += C^T P^T (M=128 latent coords per chunk, N=64 rows, K=64 tokens)
+// O is kept transposed in TMEM (latent coordinate = lane, row = column): 64 rows
+// x 512 latents take 256 of the 512 TMEM columns, leaving room for two S
+// buffers.  The running max only moves when a tile's max exceeds it by more
+// than 2^8 (normalised logits are bounded, so after the first tile this almost
+// never happens); then O is rescaled in TMEM.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads (and owns the TMEM
+// allocation), warp 1 issues MMAs, warps 2-5 do the softmax, the rescale and
+// the epilogue.  Every wait is bounded; on expiry QKMLA_ERR_TIMEOUT is recorded.
+//
+// A device-side scheduler turns seq_lens into work items (sequence, tile
+// range); long sequences are split and merged afterwards by a combine kernel.
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace qkmla {
-int launch_decode_tc(const qkmla_decode_args*, const DecodePlan&, cudaStream_t) { return QKMLA_ERR_UNSUPPORTED; }
+
+namespace {
+
+using namespace tc;
+
+constexpr int kTile = 64;          // tokens per tile
+constexpr int kRowsMMA = 64;       // M of the logit MMA
+constexpr int kThreads = 192;
+constexpr int kMaxG = 8;
+constexpr int kMaxB = 4096;
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s bound on any single wait
+
+struct WorkItem {
+    int b;
+    int tile_begin;
+    int tile_end;
+    int part;          // -1: the item is the whole sequence, write the final row
+};
+
+struct TcParams {
+    const __nv_bfloat16* qt;   // [B][s_q][H][d_c]
+    const float* aq;           // [B][s_q][H]
+    const float* qr;           // [B][s_q][H][d_r]
+    const float* grq;          // [d_r] or null
+    const float* ak;           // [num_slots][G]
+    const int32_t* seq_lens;
+    const int32_t* page_table;
+    int64_t num_pages;
+    int page_size, max_pages;
+    int B, s_q, H, G;
+    int rows_o;                // query rows per CTA (N of the output MMA)
+    float scale, eps;
+    const WorkItem* items;
+    const int* n_items;
+    float* o_part;             // [max_items][s_q*H][d_c]
+    float* lse_part;           // [max_items][s_q*H]
+    void* o;
+    int o_dtype;
+    float* lse;
+    int* status;
+};
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: spins on try_wait, checks the wall clock every 256 polls.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && globaltimer() - t0 > kWaitNs) {
+            report(status, QKMLA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool named_bar_any(int pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(pred)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void named_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& ra, float& rb) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    ra = __low2float(v);
+    rb = __high2float(v);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------------------
+// shared-memory layout
+// ---------------------------------------------------------------------------
+template <int DC, int DR, int NST>
+struct Layout {
+    static constexpr int kLatBlocks = DC / 64;                     // 64-column TMA boxes
+    static constexpr int kRopeRowBytes = DR * 2;                   // 128 (SW128) or 64 (SW64)
+    static constexpr int kQLat = kLatBlocks * kRowsMMA * 128;
+    static constexpr int kQRope = kRowsMMA * kRopeRowBytes;
+    static constexpr int kSLat = kLatBlocks * kTile * 128;
+    static constexpr int kSRope = kTile * kRopeRowBytes;
+    static constexpr int kSAk = kTile * kMaxG * 4;
+    static constexpr int kStage = ((kSLat + kSRope + kSAk) + 1023) / 1024 * 1024;
+    static constexpr int kQ = ((kQLat + kQRope) + 1023) / 1024 * 1024;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffStage = kQ;
+    static constexpr int kOffMisc = kQ + NST * kStage;
+    // misc: barriers then per-row arrays
+    static constexpr int kNumBars = 3 * NST + 5;
+    static constexpr int kMisc = kNumBars * 8 + 16 + 4 * kRowsMMA * 4;
+    static constexpr int kBytes = kOffMisc + kMisc + 1024;        // + alignment slack
+    static constexpr uint32_t kStageTx = (uint32_t)(kSLat + kSRope);
+};
+
+// TMEM columns: S_c[2] at 0/64, S_r[2] at 128/192, O^T chunks from 256.
+constexpr uint32_t kColSc = 0, kColSr = 128, kColO = 256, kTmemCols = 512;
+
+template <int DC, int DR, bool PLAIN, int NST>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
+                 const TcParams p) {
+    using LY = Layout<DC, DR, NST>;
+    constexpr int kChunks = DC / 128;
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sQ = sm + LY::kOffQ;
+    uint64_t* bars = (uint64_t*)(sm + LY::kOffMisc);
+    uint64_t* full = bars;                 // [NST] TMA -> MMA
+    uint64_t* empty = bars + NST;          // [NST] output MMA done -> TMA
+    uint64_t* pfull = bars + 2 * NST;      // [NST] P written -> output MMA
+    uint64_t* sfull = bars + 3 * NST;      // [2]  logit MMA done -> softmax
+    uint64_t* sfree = bars + 3 * NST + 2;  // [2]  softmax read S -> MMA
+    uint64_t* odone = bars + 3 * NST + 4;  // output MMA of a tile done
+    uint32_t* tmem_slot = (uint32_t*)(bars + LY::kNumBars);
+    int* abort_flag = (int*)(tmem_slot + 1);
+    float* coef_s = (float*)(sm + LY::kOffMisc + LY::kNumBars * 8 + 16);
+    float* corr_s = coef_s + kRowsMMA;
+    float* l_s = corr_s + kRowsMMA;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int item_idx = blockIdx.y;
+    if (item_idx >= *p.n_items) return;
+    const WorkItem it = p.items[item_idx];
+    const int rows_o = p.rows_o;
+    const int row0 = blockIdx.x * rows_o;          // row index within the sequence's s_q*H rows
+    const int qi = row0 / p.H, h0 = row0 % p.H;
+    const int b = it.b;
+    const int seq_len = p.seq_lens[b];
+    const bool bad = seq_len < p.s_q || seq_len > p.max_pages * p.page_size;
+    const int L = bad ? 0 : seq_len - p.s_q + qi + 1;
+    const int tiles = (L + kTile - 1) / kTile;
+    const int jt0 = it.tile_begin;
+    const int jt1 = min(it.tile_end, tiles);
+    const int n_t = max(0, jt1 - jt0);
+    const int hpg = p.H / p.G;
+
+    if (tid == 0) {
+        if (bad) report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
+        for (int s = 0; s < LY::kNumBars; ++s) {
+            uint32_t cnt = 1;
+            if (s >= 2 * NST && s < 3 * NST) cnt = 4;          // pfull: one arrive per softmax warp
+            if (s == 3 * NST + 2 || s == 3 * NST + 3) cnt = 4; // sfree
+            mbar_init(&bars[s], cnt);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&tm_lat);
+        if (DR != 64) prefetch_tmap(&tm_rope);
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+
+    // ---- prologue (softmax warps): stage Q~ and the normalised RoPE query ----
+    if (warp >= 2) {
+        const int st = tid - 64;
+        const size_t qrow0 = ((size_t)b * p.s_q + qi) * p.H + h0;
+        for (int e = st; e < kRowsMMA * (DC / 8); e += 128) {
+            const int r = e / (DC / 8), k = e % (DC / 8);
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r < rows_o) v = *reinterpret_cast<const uint4*>(p.qt + (qrow0 + r) * DC + k * 8);
+            *reinterpret_cast<uint4*>(sQ + (k >> 3) * (kRowsMMA * 128) + sw128_offset(r, (k & 7) * 8)) = v;
+        }
+        // RoPE query: two threads per row
+        {
+            const int r = st >> 1, half = st & 1;
+            float ss = 0.f;
+            float vals[DR / 2];
+            const float* src = p.qr + (qrow0 + r) * DR + half * (DR / 2);
+#pragma unroll
+            for (int j = 0; j < DR / 2; ++j) {
+                vals[j] = (r < rows_o) ? src[j] : 0.f;
+                ss = fmaf(vals[j], vals[j], ss);
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            const float beta = PLAIN ? 1.f : 1.f / sqrtf(ss / (float)DR + p.eps);
+            uint8_t* qrope = sQ + LY::kQLat;
+#pragma unroll
+            for (int j = 0; j < DR / 2; j += 2) {
+                const int c = half * (DR / 2) + j;
+                const float g0 = (PLAIN || !p.grq) ? 1.f : p.grq[c];
+                const float g1 = (PLAIN || !p.grq) ? 1.f : p.grq[c + 1];
+                __nv_bfloat162 v = __floats2bfloat162_rn(vals[j] * g0 * beta, vals[j + 1] * g1 * beta);
+                const uint32_t off = (DR == 64) ? sw128_offset(r, c) : sw64_offset(r, c);
+                *reinterpret_cast<__nv_bfloat162*>(qrope + off) = v;
+            }
+            if (half == 0) {
+                const float a = (PLAIN || r >= rows_o) ? 1.f : p.aq[qrow0 + r];
+                coef_s[r] = p.scale * a * kLog2e;
+            }
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ===================== TMA producer =====================
+        if (lane == 0) {
+            for (int j = 0; j < n_t; ++j) {
+                const int s = j % NST;
+                if (j >= NST && !wait_bounded(&empty[s], ((j / NST) - 1) & 1, p.status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*(volatile int*)abort_flag) break;
+                const int t0 = (jt0 + j) * kTile;
+                const int pg = t0 / p.page_size;
+                int64_t page = p.page_table ? (int64_t)p.page_table[(int64_t)b * p.max_pages + pg]
+                                            : (int64_t)b * p.max_pages + pg;
+                if (page < 0 || page >= p.num_pages) {
+                    report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
+                    page = 0;
+                }
+                const int64_t slot0 = page * p.page_size + (t0 % p.page_size);
+                uint8_t* stg = sm + LY::kOffStage + s * LY::kStage;
+                mbar_arrive_expect_tx(&full[s], LY::kStageTx + (PLAIN ? 0u : (uint32_t)(kTile * p.G * 4)));
+#pragma unroll
+                for (int blk = 0; blk < LY::kLatBlocks; ++blk)
+                    tma_load_2d(stg + blk * (kTile * 128), &tm_lat, blk * 64, (int)slot0, &full[s]);
+                if (DR == 64)
+                    tma_load_2d(stg + LY::kSLat, &tm_lat, DC, (int)slot0, &full[s]);
+                else
+                    tma_load_2d(stg + LY::kSLat, &tm_rope, DC, (int)slot0, &full[s]);
+                if (!PLAIN)
+                    bulk_load(stg + LY::kSLat + LY::kSRope, p.ak + slot0 * p.G, (uint32_t)(kTile * p.G * 4),
+                              &full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer =====================
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16(kRowsMMA, kTile, 0, 0);
+            const uint32_t id_o = idesc_bf16(128, rows_o, 1, 0);
+            const uint32_t q_addr = smem_u32(sQ);
+            auto issue_o = [&](int jj) -> bool {
+                const int s = jj % NST;
+                if (!wait_bounded(&pfull[s], (jj / NST) & 1, p.status)) return false;
+                tc_fence_after();
+                const uint32_t st_addr = smem_u32(sm + LY::kOffStage + s * LY::kStage);
+                const uint32_t p_addr = st_addr + LY::kSLat;       // P^T lives in the RoPE slot
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        // A = C^T chunk c: MN-major, two 64-column boxes (LBO = box stride),
+                        // 8-token groups 1024 B apart (SBO); B = P^T rows, K-major.
+                        const uint64_t a = smem_desc(st_addr + (2 * c) * (kTile * 128) + kk * 2048,
+                                                     kTile * 128, 1024, kSwizzle128B);
+                        const uint64_t bdesc = smem_desc(p_addr + kk * 32, 16, 1024, kSwizzle128B);
+                        mma_bf16(tmem + kColO + c * rows_o, a, bdesc, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(&empty[s]);
+                mma_commit(odone);
+                return true;
+            };
+            bool ok = true;
+            for (int j = 0; j < n_t && ok; ++j) {
+                const int s = j % NST, sb = j & 1;
+                if (!wait_bounded(&full[s], (j / NST) & 1, p.status)) { ok = false; break; }
+                if (j >= 2 && !wait_bounded(&sfree[sb], ((j >> 1) - 1) & 1, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t st_addr = smem_u32(sm + LY::kOffStage + s * LY::kStage);
+                const uint32_t d_c = tmem + kColSc + sb * 64;
+                const uint32_t d_r = tmem + kColSr + sb * 64;
+#pragma unroll
+                for (int blk = 0; blk < LY::kLatBlocks; ++blk) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = smem_desc(q_addr + blk * (kRowsMMA * 128) + kk * 32, 16, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(st_addr + blk * (kTile * 128) + kk * 32, 16, 1024, kSwizzle128B);
+                        mma_bf16(d_c, a, bd, id_s, (blk > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+#pragma unroll
+                for (int kk = 0; kk < DR / 16; ++kk) {
+                    uint64_t a, bd;
+                    if (DR == 64) {
+                        a = smem_desc(q_addr + LY::kQLat + kk * 32, 16, 1024, kSwizzle128B);
+                        bd = smem_desc(st_addr + LY::kSLat + kk * 32, 16, 1024, kSwizzle128B);
+                    } else {
+                        a = smem_desc(q_addr + LY::kQLat + kk * 32, 16, 512, kSwizzle64B);
+                        bd = smem_desc(st_addr + LY::kSLat + kk * 32, 16, 512, kSwizzle64B);
+                    }
+                    if (!PLAIN) {
+                        mma_bf16(d_r, a, bd, id_s, kk > 0 ? 1u : 0u);
+                    } else {
+                        mma_bf16(d_c, a, bd, id_s, 1u);      // plain MLA: one accumulation over K = d_c + d_r
+                    }
+                }
+                mma_commit(&sfull[sb]);
+                if (j >= 1) ok = issue_o(j - 1);
+            }
+            if (ok && n_t > 0) ok = issue_o(n_t - 1);
+            if (!ok) *(volatile int*)abort_flag = 1;
+        }
+    } else {
+        // ===================== softmax / rescale / epilogue =====================
+        const int sub = warp & 3;                      // TMEM sub-partition of this warp
+        const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
+        // M=64 accumulator layout: row r sits in lane r%16 of sub-partition r/16
+        const int r = 16 * sub + lane;
+        const bool row_ok = lane < 16 && r < rows_o;
+        const int g = row_ok ? ((h0 + r) % p.H) / hpg : 0;
+        const float coef = row_ok ? coef_s[r] : 0.f;
+        const float rs = p.scale * kLog2e;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_t; ++j) {
+            const int s = j % NST, sb = j & 1;
+            const int tile = jt0 + j;
+            // every abort decision is made uniformly across the four softmax warps so
+            // that none of them is left waiting at a named barrier
+            const bool got_s = wait_bounded(&sfull[sb], (j >> 1) & 1, p.status);
+            if (named_bar_any(!got_s)) { ok = false; break; }
+            tc_fence_after();
+            uint8_t* stg = sm + LY::kOffStage + s * LY::kStage;
+            const float* ak_t = (const float*)(stg + LY::kSLat + LY::kSRope);
+            const int valid = min(kTile, L - tile * kTile);
+            float lg[kTile];
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kTile / 16; ++c) {
+                uint32_t sc[16], sr[16];
+                tmem_ld16(tmem + kColSc + sb * 64 + lane_base + 16 * c, sc);
+                if (!PLAIN) tmem_ld16(tmem + kColSr + sb * 64 + lane_base + 16 * c, sr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int t = 16 * c + jj;
+                    float v;
+                    if (PLAIN) {
+                        v = rs * __uint_as_float(sc[jj]);
+                    } else {
+                        v = fmaf(coef * ak_t[t * p.G + g], __uint_as_float(sc[jj]), rs * __uint_as_float(sr[jj]));
+                    }
+                    v = (t < valid) ? v : -INFINITY;
+                    lg[t] = v;
+                    mt = fmaxf(mt, v);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sfree[sb]);
+            // lazy running max: move it only when the tile max exceeds it by > 8 (log2)
+            float corr = 1.f;
+            int need = 0;
+            if (row_ok && mt > m_run + 8.f) {
+                const float mn = mt;
+                corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mn);
+                m_run = mn;
+                need = (j > 0) ? 1 : 0;
+            }
+            if (lane < 16 && r < kRowsMMA) corr_s[r] = row_ok ? corr : 1.f;
+            const bool any = named_bar_any(need);
+            if (any) {
+                // rescale O^T columns (rows) in TMEM once the previous output MMA is done
+                const bool got_o = wait_bounded(odone, (j - 1) & 1, p.status);
+                if (named_bar_any(!got_o)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < kChunks; ++c) {
+                    for (int c16 = 0; c16 < rows_o; c16 += 16) {
+                        uint32_t v[16];
+                        const uint32_t ta = tmem + kColO + c * rows_o + c16 + lane_base;
+                        tmem_ld16(ta, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            v[jj] = __float_as_uint(__uint_as_float(v[jj]) * corr_s[c16 + jj]);
+                        tmem_st16(ta, v);
+                    }
+                }
+                tmem_wait_st();
+                // corr_s is rewritten by the next tile: every thread must be done reading it
+                named_bar_sync();
+            }
+            l_run *= corr;
+            // P^T row r: 64 tokens (128 B) into the RoPE slot of this stage, 128-byte swizzle
+            uint8_t* pT = stg + LY::kSLat;
+            float psum = 0.f;
+#pragma unroll
+            for (int k8 = 0; k8 < kTile / 8; ++k8) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int t = 8 * k8 + 2 * q;
+                    const float e0 = (lg[t] == -INFINITY) ? 0.f : exp2f(lg[t] - m_run);
+                    const float e1 = (lg[t + 1] == -INFINITY) ? 0.f : exp2f(lg[t + 1] - m_run);
+                    float r0, r1;
+                    w4[q] = pack_bf16(e0, e1, r0, r1);
+                    psum += r0 + r1;
+                }
+                if (row_ok)
+                    *reinterpret_cast<uint4*>(pT + sw128_offset(r, 8 * k8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            l_run += psum;
+            // the last tile of the sequence: zero the latent rows past its end so that
+            // stale slot contents (possibly NaN) cannot reach the output MMA
+            if (valid < kTile) {
+                const int st = tid - 64;
+                const int nrow = kTile - valid;
+                for (int e = st; e < nrow * LY::kLatBlocks * 8; e += 128) {
+                    const int rr = valid + e / (LY::kLatBlocks * 8);
+                    const int rem = e % (LY::kLatBlocks * 8);
+                    *reinterpret_cast<uint4*>(stg + (rem >> 3) * (kTile * 128) + rr * 128 + (rem & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pfull[s]);
+        }
+        // ---- epilogue ----
+        const bool got_last = (ok && n_t > 0) ? wait_bounded(odone, (n_t - 1) & 1, p.status) : true;
+        if (named_bar_any(!got_last)) ok = false;
+        tc_fence_after();
+        if (!ok) *(volatile int*)abort_flag = 1;
+        if (row_ok) {
+            l_s[r] = l_run;
+            const float lse = (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+            const size_t orow = ((size_t)b * p.s_q + qi) * p.H + h0 + r;
+            if (it.part < 0) {
+                if (p.lse) p.lse[orow] = lse;
+            } else {
+                p.lse_part[(size_t)it.part * p.s_q * p.H + (size_t)qi * p.H + h0 + r] = lse;
+            }
+        }
+        named_bar_sync();
+        const size_t orow0 = ((size_t)b * p.s_q + qi) * p.H + h0;
+        float* dst_part = (it.part >= 0) ? p.o_part + ((size_t)it.part * p.s_q * p.H + (size_t)qi * p.H + h0) * DC
+                                         : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+            const int dc = c * 128 + 32 * sub + lane;
+            for (int c16 = 0; c16 < rows_o; c16 += 16) {
+                uint32_t v[16];
+                if (n_t > 0) {
+                    tmem_ld16(tmem + kColO + c * rows_o + c16 + lane_base, v);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) v[jj] = 0u;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int rr = c16 + jj;
+                    const float l = l_s[rr];
+                    const float val = (l > 0.f) ? __uint_as_float(v[jj]) / l : 0.f;
+                    if (dst_part) {
+                        dst_part[(size_t)rr * DC + dc] = val;
+                    } else if (p.o_dtype == QKMLA_F32) {
+                        ((float*)p.o)[(orow0 + rr) * DC + dc] = val;
+                    } else {
+                        ((__nv_bfloat16*)p.o)[(orow0 + rr) * DC + dc] = __float2bfloat16_rn(val);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// scheduler: seq_lens -> work items (one CTA)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024)
+sched_kernel(const int32_t* __restrict__ seq_lens, int B, int s_q, int max_len, int n_rb, int sms, int min_tiles,
+             int fixed_splits, WorkItem* __restrict__ items, int* __restrict__ n_items, int* __restrict__ seq_nsplit,
+             int* __restrict__ seq_part0, int* status) {
+    __shared__ int tiles_s[kMaxB];
+    __shared__ int ns_by_rank[kMaxB];
+    __shared__ int rank_s[kMaxB];
+    __shared__ int red[32];
+    __shared__ int s_total, s_tpi;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    int tot = 0, mx = 0;
+    for (int b = tid; b < B; b += nt) {
+        const int L = seq_lens[b];
+        int tl = 0;
+        if (L < s_q || L > max_len) {
+            report(status, QKMLA_ERR_DEVICE_BOUNDS);
+        } else {
+            tl = (L + kTile - 1) / kTile;
+        }
+        tiles_s[b] = tl;
+        tot += tl;
+        mx = max(mx, tl);
+    }
+    // block reductions (sum, max)
+    for (int o = 16; o > 0; o >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if ((tid & 31) == 0) red[tid >> 5] = tot;
+    __syncthreads();
+    if (tid == 0) {
+        int t = 0;
+        for (int w = 0; w < (nt + 31) / 32; ++w) t += red[w];
+        s_total = t;
+    }
+    __syncthreads();
+    if ((tid & 31) == 0) red[tid >> 5] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        int m = 0;
+        for (int w = 0; w < (nt + 31) / 32; ++w) m = max(m, red[w]);
+        // ideal tiles per CTA if the whole GPU shares the work evenly
+        const float ideal = (float)s_total * n_rb / (float)sms;
+        int tpi = (float)m <= 1.25f * ideal ? m : (int)ceilf(ideal);
+        s_tpi = max(max(tpi, min_tiles), 1);
+    }
+    __syncthreads();
+    const int tpi = s_tpi;
+    // rank sequences by descending tile count (longest first), ties by index
+    for (int b = tid; b < B; b += nt) {
+        const int tb = tiles_s[b];
+        int rk = 0;
+        for (int o = 0; o < B; ++o) {
+            const int to = tiles_s[o];
+            rk += (to > tb) || (to == tb && o < b);
+        }
+        rank_s[b] = rk;
+        ns_by_rank[rk] = fixed_splits > 0 ? max(1, min(fixed_splits, tb)) : max(1, (tb + tpi - 1) / tpi);
+    }
+    __syncthreads();
+    // exclusive prefix sum over ranks (single thread; B <= 4096)
+    if (tid == 0) {
+        int acc = 0;
+        for (int k = 0; k < B; ++k) {
+            const int v = ns_by_rank[k];
+            ns_by_rank[k] = acc;
+            acc += v;
+        }
+        *n_items = acc;
+    }
+    __syncthreads();
+    for (int b = tid; b < B; b += nt) {
+        const int tb = tiles_s[b];
+        const int ns = fixed_splits > 0 ? max(1, min(fixed_splits, tb)) : max(1, (tb + tpi - 1) / tpi);
+        const int per = (tb + ns - 1) / ns;
+        const int off = ns_by_rank[rank_s[b]];
+        seq_nsplit[b] = ns;
+        seq_part0[b] = off;
+        for (int k = 0; k < ns; ++k) {
+            WorkItem w;
+            w.b = b;
+            w.tile_begin = k * per;
+            w.tile_end = min(tb, (k + 1) * per);
+            w.part = (ns > 1) ? off + k : -1;
+            items[off + k] = w;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// combine for variable split counts
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128)
+combine_var_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                   const int* __restrict__ seq_nsplit, const int* __restrict__ seq_part0, int rows_per_seq, int d_c,
+                   void* __restrict__ o, int o_dtype, float* __restrict__ lse) {
+    __shared__ float w_s[256];
+    __shared__ float s_inv, s_lse;
+    const int row = blockIdx.x;                 // (b, i, h)
+    const int b = row / rows_per_seq, rr = row % rows_per_seq;
+    const int ns = seq_nsplit[b];
+    if (ns <= 1) return;
+    const int p0 = seq_part0[b];
+    const int tid = threadIdx.x;
+    if (tid < 32) {
+        float m = -INFINITY;
+        for (int s = tid; s < ns; s += 32) m = fmaxf(m, lse_part[(size_t)(p0 + s) * rows_per_seq + rr]);
+        m = warp_max(m);
+        float sum = 0.f;
+        for (int s = tid; s < ns; s += 32) {
+            const float w = (m == -INFINITY) ? 0.f : expf(lse_part[(size_t)(p0 + s) * rows_per_seq + rr] - m);
+            if (s < 256) w_s[s] = w;
+            sum += w;
+        }
+        sum = warp_sum(sum);
+        if (tid == 0) {
+            s_inv = sum > 0.f ? 1.f / sum : 0.f;
+            s_lse = sum > 0.f ? m + logf(sum) : -INFINITY;
+        }
+    }
+    __syncthreads();
+    const float inv = s_inv;
+    for (int k = tid; k < d_c; k += 128) {
+        float acc = 0.f;
+        for (int s = 0; s < ns; ++s) {
+            const float w = w_s[s];
+            if (w != 0.f) acc = fmaf(w, o_part[((size_t)(p0 + s) * rows_per_seq + rr) * d_c + k], acc);
+        }
+        acc *= inv;
+        if (o_dtype == QKMLA_F32)
+            ((float*)o)[(size_t)row * d_c + k] = acc;
+        else
+            ((__nv_bfloat16*)o)[(size_t)row * d_c + k] = __float2bfloat16_rn(acc);
+    }
+    if (tid == 0 && lse) lse[row] = s_lse;
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int row_elems, int box_cols, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kTile};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int DC, int DR, bool PLAIN, int NST>
+int launch_kernel(const CUtensorMap& lat, const CUtensorMap& rope, const TcParams& tp, int n_rb, int max_items,
+                  cudaStream_t s) {
+    using LY = Layout<DC, DR, NST>;
+    auto k = decode_tc_kernel<DC, DR, PLAIN, NST>;
+    static_assert(LY::kBytes <= 232448, "shared memory budget");
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes) != cudaSuccess)
+        return QKMLA_ERR_CUDA;
+    dim3 grid(n_rb, max_items);
+    k<<<grid, kThreads, LY::kBytes, s>>>(lat, rope, tp);
+    return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
+}
+
+}  // namespace
+
+// Shapes the tensor-core kernel is built for (bf16 cache).
+bool tc_supported(const qkmla_decode_args* a) {
+    if (a->cache_dtype != QKMLA_BF16) return false;
+    if (!((a->d_c == 512 && a->d_r == 64) || (a->d_c == 256 && a->d_r == 32))) return false;
+    if (a->G > kMaxG || a->B > kMaxB) return false;
+    if (a->page_size % kTile) return false;
+    const int rows_o = a->H < 64 ? a->H : 64;
+    if (rows_o % 16 || a->H % rows_o) return false;
+    if (((uintptr_t)a->kv_cache % 16) || ((uintptr_t)a->q_tilde % 16)) return false;
+    if (!(a->flags & QKMLA_FLAG_PLAIN_MLA) && ((uintptr_t)a->ak_cache % 16)) return false;
+    return true;
+}
+
+size_t tc_workspace(const qkmla_decode_args* a, int sms, int* max_items_out) {
+    const int rows_o = a->H < 64 ? a->H : 64;
+    const int n_rb = a->s_q * a->H / rows_o;
+    const int target = (sms + n_rb - 1) / n_rb;
+    int max_items = a->B + target + 1;
+    if (a->num_splits > 0) max_items = a->B * a->num_splits;
+    if (max_items_out) *max_items_out = max_items;
+    size_t off = 0;
+    off += (size_t)max_items * sizeof(WorkItem);
+    off += 16 + 2 * (size_t)a->B * sizeof(int);
+    off = (off + 255) & ~(size_t)255;
+    off += (size_t)max_items * a->s_q * a->H * a->d_c * sizeof(float);
+    off += (size_t)max_items * a->s_q * a->H * sizeof(float);
+    return off + 256;
+}
+
+int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStream_t s) {
+    const int sms = device_sm_count();
+    int max_items = 0;
+    tc_workspace(a, sms, &max_items);
+    const int rows_o = a->H < 64 ? a->H : 64;
+    const int n_rb = a->s_q * a->H / rows_o;
+    uint8_t* ws = (uint8_t*)a->workspace;
+    WorkItem* items = (WorkItem*)ws;
+    size_t off = (size_t)max_items * sizeof(WorkItem);
+    int* n_items = (int*)(ws + off);
+    int* seq_nsplit = n_items + 4;
+    int* seq_part0 = seq_nsplit + a->B;
+    off += 16 + 2 * (size_t)a->B * sizeof(int);
+    off = (off + 255) & ~(size_t)255;
+    float* o_part = (float*)(ws + off);
+    float* lse_part = o_part + (size_t)max_items * a->s_q * a->H * a->d_c;
+    int* status = device_status_ptr();
+    const int max_len = a->max_pages * a->page_size;
+
+    sched_kernel<<<1, 1024, 0, s>>>(a->seq_lens, a->B, a->s_q, max_len, n_rb, sms, /*min_tiles=*/8, a->num_splits,
+                                    items, n_items, seq_nsplit, seq_part0, status);
+    if (cudaGetLastError() != cudaSuccess) return QKMLA_ERR_CUDA;
+
+    CUtensorMap lat, rope;
+    const int row = a->d_c + a->d_r;
+    if (!make_map(&lat, a->kv_cache, a->num_slots, row, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return QKMLA_ERR_CUDA;
+    if (a->d_r == 64) {
+        rope = lat;
+    } else if (!make_map(&rope, a->kv_cache, a->num_slots, row, 32, CU_TENSOR_MAP_SWIZZLE_64B)) {
+        return QKMLA_ERR_CUDA;
+    }
+    TcParams tp;
+    tp.qt = (const __nv_bfloat16*)a->q_tilde;
+    tp.aq = a->alpha_q;
+    tp.qr = a->q_rope;
+    tp.grq = a->gamma_rope_q;
+    tp.ak = a->ak_cache;
+    tp.seq_lens = a->seq_lens;
+    tp.page_table = a->page_table;
+    tp.num_pages = a->num_slots / a->page_size;
+    tp.page_size = a->page_size;
+    tp.max_pages = a->max_pages;
+    tp.B = a->B; tp.s_q = a->s_q; tp.H = a->H; tp.G = a->G;
+    tp.rows_o = rows_o;
+    tp.scale = a->softmax_scale;
+    tp.eps = a->eps;
+    tp.items = items;
+    tp.n_items = n_items;
+    tp.o_part = o_part;
+    tp.lse_part = lse_part;
+    tp.o = a->o;
+    tp.o_dtype = a->o_dtype;
+    tp.lse = a->lse;
+    tp.status = status;
+    const bool plain = (a->flags & QKMLA_FLAG_PLAIN_MLA) != 0;
+    int rc;
+    if (a->d_c == 512) {
+        rc = plain ? launch_kernel<512, 64, true, 2>(lat, rope, tp, n_rb, max_items, s)
+                   : launch_kernel<512, 64, false, 2>(lat, rope, tp, n_rb, max_items, s);
+    } else {
+        rc = plain ? launch_kernel<256, 32, true, 4>(lat, rope, tp, n_rb, max_items, s)
+                   : launch_kernel<256, 32, false, 4>(lat, rope, tp, n_rb, max_items, s);
+    }
+    if (rc != QKMLA_OK) return rc;
+    combine_var_kernel<<<a->B * a->s_q * a->H, 128, 0, s>>>(o_part, lse_part, seq_nsplit, seq_part0, a->s_q * a->H,
+                                                             a->d_c, a->o, a->o_dtype, a->lse);
+    return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
+}
+
 }  // namespace qkmla
