@@ -8,12 +8,12 @@
 // into the attention path.  Values are the latents (latent decode path).
 //
 // Work decomposition.  A CTA owns 64 query rows (heads of one query token) of
-// one sequence and a contiguous range of 64-token tiles.  Per tile:
-//   S_c = Q~ C^T   (M=64 rows, N=64 tokens, K=d_c)   tcgen05, fp32 in TMEM
-//   S_r = Q^r K^rT (M=64,      N=64,        K=d_r)   tcgen05, fp32 in TMEM
+// one sequence and a contiguous range of 32-token tiles.  Per tile:
+//   S_c = Q~ C^T   (M=64 rows, N=32 tokens, K=d_c)   tcgen05, fp32 in TMEM
+//   S_r = Q^r K^rT (M=64,      N=32,        K=d_r)   tcgen05, fp32 in TMEM
 //   l   = scale*(alpha^q_row * alpha^k_{t,g(row)} * S_c + S_r)      (fused, fp32)
 //   P   = exp2(l*log2e - m_row), stored bf16 into the tile's RoPE slot
-//   O^T += C^T P^T (M=128 latent coords per chunk, N=64 rows, K=64 tokens)
+//   O^T += C^T P^T (M=128 latent coords per chunk, N=64 rows, K=32 tokens)
 // O is kept transposed in TMEM (latent coordinate = lane, row = column): 64 rows
 // x 512 latents take 256 of the 512 TMEM columns, leaving room for two S
 // buffers.  The running max only moves when a tile's max exceeds it by more
@@ -37,7 +37,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kTile = 64;          // tokens per tile
+constexpr int kTile = 32;          // tokens per tile (a page holds a whole number of tiles)
 constexpr int kRowsMMA = 64;       // M of the logit MMA
 constexpr int kThreads = 192;
 constexpr int kMaxG = 8;
@@ -138,8 +138,8 @@ struct Layout {
     static constexpr uint32_t kStageTx = (uint32_t)(kSLat + kSRope);
 };
 
-// TMEM columns: S_c[2] at 0/64, S_r[2] at 128/192, O^T chunks from 256.
-constexpr uint32_t kColSc = 0, kColSr = 128, kColO = 256, kTmemCols = 512;
+// TMEM columns: S_c[2] at 0/32, S_r[2] at 64/96, O^T chunks from 256.
+constexpr uint32_t kColSc = 0, kColSr = 64, kColO = 256, kTmemCols = 512;
 
 template <int DC, int DR, bool PLAIN, int NST>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -296,7 +296,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                         // 8-token groups 1024 B apart (SBO); B = P^T rows, K-major.
                         const uint64_t a = smem_desc(st_addr + (2 * c) * (kTile * 128) + kk * 2048,
                                                      kTile * 128, 1024, kSwizzle128B);
-                        const uint64_t bdesc = smem_desc(p_addr + kk * 32, 16, 1024, kSwizzle128B);
+                        const uint64_t bdesc = smem_desc(p_addr + kk * 32, 16, 512, kSwizzle64B);
                         mma_bf16(tmem + kColO + c * rows_o, a, bdesc, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
@@ -311,8 +311,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                 if (j >= 2 && !wait_bounded(&sfree[sb], ((j >> 1) - 1) & 1, p.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t st_addr = smem_u32(sm + LY::kOffStage + s * LY::kStage);
-                const uint32_t d_c = tmem + kColSc + sb * 64;
-                const uint32_t d_r = tmem + kColSr + sb * 64;
+                const uint32_t d_c = tmem + kColSc + sb * kTile;
+                const uint32_t d_r = tmem + kColSr + sb * kTile;
 #pragma unroll
                 for (int blk = 0; blk < LY::kLatBlocks; ++blk) {
 #pragma unroll
@@ -359,10 +359,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
         for (int j = 0; j < n_t; ++j) {
             const int s = j % NST, sb = j & 1;
             const int tile = jt0 + j;
-            // every abort decision is made uniformly across the four softmax warps so
-            // that none of them is left waiting at a named barrier
+            // a timed-out wait is folded into the per-tile vote below, so every abort
+            // decision is uniform across the four softmax warps (none is left at a
+            // named barrier)
             const bool got_s = wait_bounded(&sfull[sb], (j >> 1) & 1, p.status);
-            if (named_bar_any(!got_s)) { ok = false; break; }
+            if (!got_s) *(volatile int*)abort_flag = 1;
             tc_fence_after();
             uint8_t* stg = sm + LY::kOffStage + s * LY::kStage;
             const float* ak_t = (const float*)(stg + LY::kSLat + LY::kSRope);
@@ -372,8 +373,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
 #pragma unroll
             for (int c = 0; c < kTile / 16; ++c) {
                 uint32_t sc[16], sr[16];
-                tmem_ld16(tmem + kColSc + sb * 64 + lane_base + 16 * c, sc);
-                if (!PLAIN) tmem_ld16(tmem + kColSr + sb * 64 + lane_base + 16 * c, sr);
+                tmem_ld16(tmem + kColSc + sb * kTile + lane_base + 16 * c, sc);
+                if (!PLAIN) tmem_ld16(tmem + kColSr + sb * kTile + lane_base + 16 * c, sr);
                 tmem_wait_ld();
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
@@ -402,7 +403,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                 need = (j > 0) ? 1 : 0;
             }
             if (lane < 16 && r < kRowsMMA) corr_s[r] = row_ok ? corr : 1.f;
-            const bool any = named_bar_any(need);
+            const bool any = named_bar_any(need || !got_s);
+            if (any && *(volatile int*)abort_flag) { ok = false; break; }
             if (any) {
                 // rescale O^T columns (rows) in TMEM once the previous output MMA is done
                 const bool got_o = wait_bounded(odone, (j - 1) & 1, p.status);
@@ -426,7 +428,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                 named_bar_sync();
             }
             l_run *= corr;
-            // P^T row r: 64 tokens (128 B) into the RoPE slot of this stage, 128-byte swizzle
+            // P^T row r: 32 tokens (64 B) into the RoPE slot of this stage, 64-byte swizzle
             uint8_t* pT = stg + LY::kSLat;
             float psum = 0.f;
 #pragma unroll
@@ -442,7 +444,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                     psum += r0 + r1;
                 }
                 if (row_ok)
-                    *reinterpret_cast<uint4*>(pT + sw128_offset(r, 8 * k8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    *reinterpret_cast<uint4*>(pT + sw64_offset(r, 8 * k8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
             l_run += psum;
             // the last tile of the sequence: zero the latent rows past its end so that
@@ -709,6 +711,7 @@ bool tc_supported(const qkmla_decode_args* a) {
     if (a->page_size % kTile) return false;
     const int rows_o = a->H < 64 ? a->H : 64;
     if (rows_o % 16 || a->H % rows_o) return false;
+    if (rows_o > a->d_r) return false;     // P^T (rows_o x 32 tokens) reuses the tile's RoPE slot
     if (((uintptr_t)a->kv_cache % 16) || ((uintptr_t)a->q_tilde % 16)) return false;
     if (!(a->flags & QKMLA_FLAG_PLAIN_MLA) && ((uintptr_t)a->ak_cache % 16)) return false;
     return true;
@@ -749,7 +752,7 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     int* status = device_status_ptr();
     const int max_len = a->max_pages * a->page_size;
 
-    sched_kernel<<<1, 1024, 0, s>>>(a->seq_lens, a->B, a->s_q, max_len, n_rb, sms, /*min_tiles=*/8, a->num_splits,
+    sched_kernel<<<1, 1024, 0, s>>>(a->seq_lens, a->B, a->s_q, max_len, n_rb, sms, /*min_tiles=*/16, a->num_splits,
                                     items, n_items, seq_nsplit, seq_part0, status);
     if (cudaGetLastError() != cudaSuccess) return QKMLA_ERR_CUDA;
 
@@ -787,11 +790,11 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     const bool plain = (a->flags & QKMLA_FLAG_PLAIN_MLA) != 0;
     int rc;
     if (a->d_c == 512) {
-        rc = plain ? launch_kernel<512, 64, true, 2>(lat, rope, tp, n_rb, max_items, s)
-                   : launch_kernel<512, 64, false, 2>(lat, rope, tp, n_rb, max_items, s);
+        rc = plain ? launch_kernel<512, 64, true, 4>(lat, rope, tp, n_rb, max_items, s)
+                   : launch_kernel<512, 64, false, 4>(lat, rope, tp, n_rb, max_items, s);
     } else {
-        rc = plain ? launch_kernel<256, 32, true, 4>(lat, rope, tp, n_rb, max_items, s)
-                   : launch_kernel<256, 32, false, 4>(lat, rope, tp, n_rb, max_items, s);
+        rc = plain ? launch_kernel<256, 32, true, 8>(lat, rope, tp, n_rb, max_items, s)
+                   : launch_kernel<256, 32, false, 8>(lat, rope, tp, n_rb, max_items, s);
     }
     if (rc != QKMLA_OK) return rc;
     combine_var_kernel<<<a->B * a->s_q * a->H, 128, 0, s>>>(o_part, lse_part, seq_nsplit, seq_part0, a->s_q * a->H,

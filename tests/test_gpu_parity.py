@@ -226,9 +226,10 @@ def test_decode_split_counts_agree(Q, splits, simt):
     o_ref, lse_ref = OR.reference(w)
     check_close(_np(st.o), o_ref, "bf16", f"splits={splits} o", edge=True)
     check_close(_np(st.lse), lse_ref, "bf16", f"splits={splits} lse", edge=True)
-    # different split counts only change fp32 rounding
-    assert np.max(np.abs(_np(st.o) - o_auto)) <= 1e-3
-    assert np.max(np.abs(_np(st.lse) - l_auto)) <= 1e-3
+    # different split counts change the reference maxima the bf16 P is rounded
+    # against (tensor-core kernel) or only the fp32 summation order (CUDA cores)
+    check_close(_np(st.o), o_auto, "bf16", f"splits={splits} vs auto o", edge=True)
+    check_close(_np(st.lse), l_auto, "bf16", f"splits={splits} vs auto lse", edge=True)
 
 
 def test_decode_bad_page_id_is_reported_not_trapped(Q):
