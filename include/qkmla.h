@@ -193,6 +193,30 @@ int qkmla_version(void);
  */
 const char* qkmla_decode_kernel_name(const qkmla_decode_args* a);
 
+/*
+ * qkmla_decode_noalloc -- qkmla_decode for callers that cannot allocate
+ * device memory when they decode: a runtime that hands out only pre-planned
+ * buffers, a plugin whose host owns every allocation, or a thread that must
+ * not enter the CUDA allocator.  The paper has no counterpart to this call.
+ *
+ * Same arguments and results as qkmla_decode, except that `workspace` and
+ * `workspace_bytes` are ignored: the split-KV partials and scheduler data live
+ * in a fixed array of qkmla_decode_noalloc_max_workspace() bytes (64 MiB)
+ * inside the library, held on every GPU where it is used until the process
+ * exits.  The call allocates nothing.  Arguments needing more scratch than
+ * that return QKMLA_ERR_WORKSPACE before anything is launched.
+ * The first call on a device resolves the array's address on that device (it
+ * must be current); make that first call before any stream capture.  All
+ * calls on a device share the array: calls whose kernels can overlap on the
+ * GPU (different streams with no ordering between them) race on it.  The
+ * array keeps the previous call's contents; decode writes every scratch entry
+ * it reads, so nothing needs to start at zero.
+ */
+int qkmla_decode_noalloc(const qkmla_decode_args* a, void* stream);
+
+/* Bytes of scratch qkmla_decode_noalloc can use (its fixed array). */
+size_t qkmla_decode_noalloc_max_workspace(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -91,6 +91,11 @@ def lib() -> ctypes.CDLL:
         L.qkmla_version.restype = i
         L.qkmla_decode_kernel_name.argtypes = [ctypes.POINTER(DecodeArgs)]
         L.qkmla_decode_kernel_name.restype = ctypes.c_char_p
+        if hasattr(L, "qkmla_decode_noalloc"):
+            L.qkmla_decode_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), vp]
+            L.qkmla_decode_noalloc.restype = i
+            L.qkmla_decode_noalloc_max_workspace.argtypes = []
+            L.qkmla_decode_noalloc_max_workspace.restype = sz
         _lib = L
     return _lib
 
