@@ -183,6 +183,28 @@ def cpu_oracle_rate(w: W.Workload, target_s: float):
     return toks / t_total, sample, t_total
 
 
+def rank_workload(w0: W.Workload, rank: int) -> W.Workload:
+    """Each rank decodes its own batch (same shapes, its own seed): the path
+    shards by sequence, so ranks share no data and need no collective."""
+    return w0.with_(seed=w0.seed + 7919 * rank) if rank else w0
+
+
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """Max of a per-rank timing over all ranks (the job ends with the slowest)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step: int, world: int, total_ms_max: float, steps: int) -> float:
+    """Whole-job rate: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank_step * world * steps / (total_ms_max / 1e3)
+
+
 def cpu_threads() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -226,7 +248,7 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    w = w0.with_(seed=w0.seed + 7919 * rank) if rank else w0
+    w = rank_workload(w0, rank)
 
     from qk_normed_latent_gb300 import build as B
     B.build()
@@ -275,16 +297,12 @@ def main():
     if world > 1:
         dist.barrier()
     clocks = clk.stop()
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, device="cuda")
     if Q.get_device_status() != 0:
         raise RuntimeError("device status error in the timed region")
     ms_per_step = total_ms / args.steps
     tokens_per_step = w.B * w.s_q
-    value = tokens_per_step * world / (total_ms / 1e3 / args.steps) / 1.0
+    value = job_throughput(tokens_per_step, world, total_ms, args.steps)
     dec_avg = statistics.mean(dec_ms)
 
     # roofline of the dominant kernel (the decode call: decode kernel + combine)

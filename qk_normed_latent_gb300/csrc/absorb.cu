@@ -103,6 +103,9 @@ absorb_kernel(const float* __restrict__ q, const float* __restrict__ gq, const f
 int launch_absorb(const float* q, const float* gq, const float* gk, const float* wk, int rows, int H,
                   int G, int d_h, int d_c, float eps, bool plain, void* qt, int qt_dtype, float* aq,
                   cudaStream_t s) {
+    // bf16 q~ (the tensor-core decode operand): split-bf16 tensor-core GEMM
+    if (qt_dtype == QKMLA_BF16 && absorb_tc_supported(q, wk, d_h, d_c))
+        return launch_absorb_tc(q, gq, gk, wk, rows, H, G, d_h, d_c, eps, plain, qt, qt_dtype, aq, s);
     const int M = rows * (H / G);
     dim3 grid((M + kTM - 1) / kTM, (d_c + kTN - 1) / kTN, G);
     const size_t smem = (size_t)(kTM + kTN) * (d_h + 1) * sizeof(float);

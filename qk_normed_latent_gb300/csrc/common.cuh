@@ -62,6 +62,9 @@ namespace qkmla {
 int launch_absorb(const float* q, const float* gq, const float* gk, const float* wk, int rows, int H,
                   int G, int d_h, int d_c, float eps, bool plain, void* qt, int qt_dtype, float* aq,
                   cudaStream_t s);
+bool absorb_tc_supported(const float* q, const float* wk, int d_h, int d_c);
+int launch_absorb_tc(const float* q, const float* gq, const float* gk, const float* wk, int rows, int H, int G,
+                     int d_h, int d_c, float eps, bool plain, void* qt, int qt_dtype, float* aq, cudaStream_t s);
 int launch_append(const float* c_new, const float* r_new, const float* wk, const float* grk,
                   const int64_t* slots, int N, int G, int d_c, int d_h, int d_r, float eps, bool plain,
                   void* kv, int cache_dtype, float* ak, int64_t num_slots, cudaStream_t s);

@@ -1,0 +1,189 @@
+// Device helpers shared by the tensor-core decode kernels (sm_103a).
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace qkmla {
+namespace dec {
+
+using namespace tc;
+
+constexpr int kMaxG = 8;
+constexpr int kMaxB = 4096;
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s bound on any single wait
+
+struct WorkItem {
+    int b;
+    int tile_begin;
+    int tile_end;
+    int part;          // -1: the item is the whole sequence, write the final row
+};
+
+struct TcParams {
+    const __nv_bfloat16* qt;   // [B][s_q][H][d_c]
+    const float* aq;           // [B][s_q][H]
+    const float* qr;           // [B][s_q][H][d_r]
+    const float* grq;          // [d_r] or null
+    const float* ak;           // [num_slots][G]
+    const int32_t* seq_lens;
+    const int32_t* page_table;
+    int64_t num_pages;
+    int page_size, max_pages;
+    int B, s_q, H, G;
+    int rows_o;                // query rows per CTA (N of the output MMA)
+    float scale, eps;
+    const WorkItem* items;
+    const int* n_items;
+    float* o_part;             // [max_items][s_q*H][d_c]
+    float* lse_part;           // [max_items][s_q*H]
+    void* o;
+    int o_dtype;
+    float* lse;
+    int* status;
+};
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: spins on try_wait, checks the wall clock every 256 polls.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && globaltimer() - t0 > kWaitNs) {
+            report(status, QKMLA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool named_bar_any(int pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(pred)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void named_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// 2^x with the hardware approximation (ex2.approx.ftz); 2^-inf = +0.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 16 lanes x 32 bit x 16 columns, two halves: lanes 0-15 of the warp read TMEM
+// lanes base..base+15 at columns c..c+15, lanes 16-31 the same TMEM lanes at
+// columns c+16..c+31.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], 16;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+
+// ---------------------------------------------------------------------------
+// thread-block clusters: rank, distributed shared memory, remote signalling
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+// 16-byte store into another CTA's shared memory that completes `bytes` on the
+// mbarrier at `remote_bar` (in that CTA) once the data is visible there.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c, float d,
+                                            uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(remote_addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+                 : "memory");
+}
+// Bounded wait with cluster-scope acquire (data written by the other CTA).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t parity, int* status) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((i & 255u) == 0 && globaltimer() - t0 > kWaitNs) {
+            report(status, QKMLA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+// Arrive (once) on the mbarrier at the same offset in every CTA of `cta_mask`
+// when all MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"(cta_mask)
+        : "memory");
+}
+// Bulk copy from this CTA's shared memory into another CTA's (of the cluster),
+// completing `bytes` on the mbarrier `remote_bar` there.
+__device__ __forceinline__ void bulk_copy_to_cta(uint32_t remote_dst, const void* local_src, uint32_t bytes,
+                                                 uint32_t remote_bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(remote_dst), "r"(smem_u32(local_src)), "r"(bytes), "r"(remote_bar)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk copy has finished READING its source.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Arrive once on an mbarrier of another CTA of the cluster (release, cluster scope).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+// Pull a 2-D tensor-map box into L2 ahead of its TMA load.
+__device__ __forceinline__ void tma_prefetch_l2(const void* tmap, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y)
+                 : "memory");
+}
+// Cluster-wide barrier (all threads of every CTA of the cluster).  The
+// non-aligned form: callers may arrive from diverged code paths.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Host side, shared by the launchers.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int row_elems, int box_cols, int box_rows,
+              CUtensorMapSwizzle sw);
+int launch_pair(const qkmla_decode_args* a, const TcParams& tp, int max_items, cudaStream_t s);
+}  // namespace dec
+bool pair_shape(const qkmla_decode_args* a);
+namespace dec {
+
+}  // namespace dec
+}  // namespace qkmla

@@ -1,0 +1,477 @@
+// Two-CTA cluster decode kernel for the DeepSeek-V3 decode shape
+// (d_c = 512, d_r = 64, 128 query heads per query token, bf16 cache).
+//
+// Source: "QK-Normed MLA: QK normalization without full key caching", Technical
+// Summary, Methodology -- decode-logit equation
+//     l_{i,t,h} = (q~_{i,h} . c_t) alpha^q_{i,h} alpha^k_{t,g(h)}
+// with the scalars applied as a row/column scaling before the softmax, plus the
+// separately normalised RoPE logit ("Blockwise Normalization"); values are the
+// latents (the abstract's latent decode path).
+//
+// Why a pair.  A tcgen05.mma costs about the same time for any N <= 128, so
+// the logit MMA wants M = 128 query rows; but the fp32 output of 128 rows x 512
+// latents fills all of one SM's TMEM.  The pair therefore splits the latent
+// dimension: CTA r owns latent columns [256 r, 256 r + 256) and RoPE columns
+// [32 r, 32 r + 32).  Per 64-token tile each CTA
+//   * computes partial logits over its half of K (M=128 rows, N=64, K=288),
+//     and applies the alpha^q / alpha^k scaling to its content part (the
+//     scaling is linear, so partial logits add),
+//   * exchanges partials with the other CTA: every softmax warp stages its 32
+//     rows locally and sends them with one bulk copy into the other CTA's
+//     shared memory (completing on a per-warp mbarrier there), then adds the
+//     rows it received -- fp32 addition commutes, so both CTAs hold
+//     bit-identical logits and P,
+//   * accumulates O = P C over its 256 latents (M=128 rows, N=256, K=64).
+// Each CTA streams only its half of every tile from HBM.
+//
+// Warps: 0 TMA producer (+ TMEM owner), 1 MMA issuer, 2-5 softmax / exchange /
+// epilogue (thread = query row = TMEM lane).  Softmax warps run independently
+// (each owns 32 rows end to end).  All waits are bounded (2 s).
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "decode_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace qkmla {
+namespace dec {
+namespace {
+
+constexpr int kT = 64;             // tokens per tile
+constexpr int kR = 128;            // query rows per pair
+constexpr int kDC = 512, kDR = 64;
+constexpr int kHalfLat = kDC / 2;  // latent columns per CTA
+constexpr int kHalfRope = kDR / 2; // RoPE columns per CTA
+constexpr int kThreadsP = 192;
+
+// shared memory (offsets from a 1024-byte aligned base)
+constexpr int kQLat = 4 * kR * 128;                    // Q~ half: 4 blocks of 128 rows x 128 B
+constexpr int kQRope = kR * 64;                        // RoPE half: 128 rows x 64 B (64-byte swizzle)
+constexpr int kSLat = 4 * kT * 128;                    // tile half: 4 boxes of 64 tokens x 128 B
+constexpr int kSRope = kT * 64;                        // 64 tokens x 64 B
+constexpr int kSAk = kT * kMaxG * 4;
+constexpr int kStageB = kSLat + kSRope + kSAk;         // 38 KB
+constexpr int kXB = kR * kT * 4;                       // 128 rows x 64 fp32 (8 KB per softmax warp)
+constexpr int kOffQ = 0;
+constexpr int kOffStage = kQLat + kQRope;
+constexpr int kOffX = kOffStage + 2 * kStageB;         // received partials
+constexpr int kOffY = kOffX + kXB;                     // own partials (sent), then P
+constexpr int kOffMisc = kOffY + kXB;
+constexpr int kNumBars = 19;
+constexpr int kBytesP = kOffMisc + kNumBars * 8 + 16 + kR * 4 + 1024;
+static_assert(kStageB % 1024 == 0 && kOffStage % 1024 == 0 && kOffX % 1024 == 0 && kOffY % 1024 == 0, "align");
+static_assert(kBytesP <= 232448, "shared memory budget");
+
+// TMEM columns: S_c[2] at 0/64, S_r[2] at 128/192, O (128 rows x 256 latents) at 256
+constexpr uint32_t kCSc = 0, kCSr = 128, kCO = 256;
+
+// Byte offset of floats 4k..4k+3 of row r in an exchange buffer: rows of 256 B,
+// 16-byte chunks XOR-swizzled; rows 32w..32w+31 form warp w's 8 KB slice.
+__device__ __forceinline__ uint32_t xoff(int r, int k) { return (uint32_t)(r * 256 + (((k ^ r) & 15) << 4)); }
+// P (A operand of the output MMA): K-major, 128-byte swizzle, 8-row groups
+// 2048 B apart so that warp w's 32 rows stay inside its own 8 KB slice.
+__device__ __forceinline__ uint32_t poff(int r, int col) {
+    return (uint32_t)((r >> 3) * 2048 + (r & 7) * 128 + ((((col >> 3) ^ (r & 7)) & 7) << 4) + (col & 7) * 2);
+}
+
+template <bool PLAIN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsP, 1)
+decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
+                   const TcParams p) {
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sQ = sm + kOffQ;
+    uint8_t* sX = sm + kOffX;
+    uint8_t* sY = sm + kOffY;
+    uint64_t* bars = (uint64_t*)(sm + kOffMisc);
+    uint64_t* full = bars;          // [2] TMA -> MMA
+    uint64_t* empty = bars + 2;     // [2] output MMA done -> TMA
+    uint64_t* sfull = bars + 4;     // [2] logit MMA done -> softmax
+    uint64_t* sfree = bars + 6;     // [2] softmax read S -> MMA
+    uint64_t* pfull = bars + 8;     // [2] P written -> output MMA
+    uint64_t* odone = bars + 10;    // output MMA of a tile done
+    uint64_t* xfull = bars + 11;    // [4] per warp: the other CTA's partial rows landed in X
+    uint64_t* xfree = bars + 15;    // [4] per warp: the other CTA's X rows may be overwritten
+    uint32_t* tmem_slot = (uint32_t*)(bars + kNumBars);
+    int* abort_flag = (int*)(tmem_slot + 1);
+    float* coef_s = (float*)(sm + kOffMisc + kNumBars * 8 + 16);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if ((int)blockIdx.y >= *p.n_items) return;          // uniform over the cluster
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    const WorkItem it = p.items[blockIdx.y];
+    const int qi = blockIdx.x >> 1;                       // query token of this pair
+    const int b = it.b;
+    const int seq_len = p.seq_lens[b];
+    const bool bad = seq_len < p.s_q || seq_len > p.max_pages * p.page_size;
+    const int L = bad ? 0 : seq_len - p.s_q + qi + 1;
+    const int tiles = (L + kT - 1) / kT;
+    const int jt0 = it.tile_begin;
+    const int n_t = max(0, min(it.tile_end, tiles) - jt0);
+    const int hpg = p.H / p.G;
+
+    if (tid == 0) {
+        if (bad && rank == 0) report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
+        for (int i = 0; i < kNumBars; ++i) {
+            const bool four = (i == 6 || i == 7 || i == 8 || i == 9);   // sfree, pfull: one per softmax warp
+            mbar_init(&bars[i], four ? 4u : 1u);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&tm_lat);
+        prefetch_tmap(&tm_rope);
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    // ---- prologue: this CTA's half of Q~ and of the normalised RoPE query ----
+    if (warp >= 2) {
+        const int st = tid - 64;
+        const size_t qrow0 = ((size_t)b * p.s_q + qi) * p.H;
+        for (int e = st; e < kR * (kHalfLat / 8); e += 128) {
+            const int r = e / (kHalfLat / 8), k = e % (kHalfLat / 8);    // k: 16-byte chunk in the half row
+            const uint4 v = *reinterpret_cast<const uint4*>(p.qt + (qrow0 + r) * kDC + rank * kHalfLat + k * 8);
+            *reinterpret_cast<uint4*>(sQ + (k >> 3) * (kR * 128) + sw128_offset(r, (k & 7) * 8)) = v;
+        }
+        {   // one thread per row: RMS over all 64 RoPE dims, keep this CTA's 32
+            const int r = st;
+            const float* src = p.qr + (qrow0 + r) * kDR;
+            float ss = 0.f;
+#pragma unroll 8
+            for (int j = 0; j < kDR; ++j) ss = fmaf(src[j], src[j], ss);
+            // QK mode: scale*log2e rides on the RoPE query, so its MMA output is
+            // already the RoPE logit in the exp2 domain
+            const float beta = PLAIN ? 1.f : p.scale * kLog2e / sqrtf(ss / (float)kDR + p.eps);
+            uint8_t* qrope = sQ + kQLat;
+#pragma unroll
+            for (int j = 0; j < kHalfRope; j += 2) {
+                const int c = rank * kHalfRope + j;
+                const float g0 = (PLAIN || !p.grq) ? 1.f : p.grq[c];
+                const float g1 = (PLAIN || !p.grq) ? 1.f : p.grq[c + 1];
+                const __nv_bfloat162 v = __floats2bfloat162_rn(src[c] * g0 * beta, src[c + 1] * g1 * beta);
+                *reinterpret_cast<__nv_bfloat162*>(qrope + sw64_offset(r, j)) = v;
+            }
+            coef_s[r] = PLAIN ? 0.f : p.scale * p.aq[qrow0 + r] * kLog2e;
+        }
+        fence_proxy_async_smem();
+        if (lane == 0 && n_t > 0) mbar_arrive_expect_tx(&xfull[warp & 3], kXB / 4);   // tile 0's rows
+    }
+    tc_fence_before();
+    cluster_sync();            // both CTAs' barriers exist before any remote access
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ===================== TMA producer: this CTA's half of each tile =====================
+        if (lane == 0) {
+            const uint32_t tx = (uint32_t)(kSLat + kSRope) + (PLAIN ? 0u : (uint32_t)(kT * p.G * 4));
+            auto slot_of_tile = [&](int j) -> int {
+                const int t0 = (jt0 + j) * kT;
+                const int pg = t0 / p.page_size;
+                int64_t page = p.page_table ? (int64_t)p.page_table[(int64_t)b * p.max_pages + pg]
+                                            : (int64_t)b * p.max_pages + pg;
+                if (page < 0 || page >= p.num_pages) {
+                    report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
+                    page = 0;
+                }
+                return (int)(page * p.page_size + (t0 % p.page_size));
+            };
+            for (int j = 0; j < n_t && j < 2; ++j) {       // L2 prefetch of the first tiles
+                const int sl = slot_of_tile(j);
+                for (int blk = 0; blk < 4; ++blk) tma_prefetch_l2(&tm_lat, rank * kHalfLat + blk * 64, sl);
+            }
+            for (int j = 0; j < n_t; ++j) {
+                const int s = j & 1;
+                if (j + 2 < n_t) {                          // two tiles ahead into L2
+                    const int sl = slot_of_tile(j + 2);
+                    for (int blk = 0; blk < 4; ++blk) tma_prefetch_l2(&tm_lat, rank * kHalfLat + blk * 64, sl);
+                    tma_prefetch_l2(&tm_rope, kDC + rank * kHalfRope, sl);
+                }
+                if (j >= 2 && !wait_bounded(&empty[s], ((j >> 1) - 1) & 1, p.status)) { *abort_flag = 1; break; }
+                if (*(volatile int*)abort_flag) break;
+                const int slot0 = slot_of_tile(j);
+                uint8_t* stg = sm + kOffStage + s * kStageB;
+                mbar_arrive_expect_tx(&full[s], tx);
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk)
+                    tma_load_2d(stg + blk * (kT * 128), &tm_lat, rank * kHalfLat + blk * 64, slot0, &full[s]);
+                tma_load_2d(stg + kSLat, &tm_rope, kDC + rank * kHalfRope, slot0, &full[s]);
+                if (!PLAIN) bulk_load(stg + kSLat + kSRope, p.ak + (int64_t)slot0 * p.G, (uint32_t)(kT * p.G * 4), &full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer =====================
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16(kR, kT, 0, 0);
+            const uint32_t id_o = idesc_bf16(kR, kHalfLat, 0, 1);
+            const uint32_t q_addr = smem_u32(sQ);
+            const uint32_t y_addr = smem_u32(sY);
+            auto issue_o = [&](int jj) -> bool {
+                const int s = jj & 1;
+                if (!wait_bounded(&pfull[s], (jj >> 1) & 1, p.status)) return false;
+                tc_fence_after();
+                const uint32_t st_addr = smem_u32(sm + kOffStage + s * kStageB);
+#pragma unroll
+                for (int kk = 0; kk < kT / 16; ++kk) {
+                    // A = P: K-major, 8-row groups 2048 B apart; B = C^T: this CTA's 256
+                    // latents (4 boxes, LBO = box stride) x 16 tokens (8-token groups, SBO)
+                    const uint64_t a = smem_desc(y_addr + kk * 32, 16, 2048, kSwizzle128B);
+                    const uint64_t bd = smem_desc(st_addr + kk * 2048, kT * 128, 1024, kSwizzle128B);
+                    mma_bf16(tmem + kCO, a, bd, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&empty[s]);
+                mma_commit(odone);
+                return true;
+            };
+            bool ok = true;
+            for (int j = 0; j < n_t && ok; ++j) {
+                const int s = j & 1;
+                if (!wait_bounded(&full[s], (j >> 1) & 1, p.status)) { ok = false; break; }
+                if (j >= 2 && !wait_bounded(&sfree[s], ((j >> 1) - 1) & 1, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t st_addr = smem_u32(sm + kOffStage + s * kStageB);
+                const uint32_t d_c = tmem + kCSc + s * kT;
+                const uint32_t d_r = tmem + kCSr + s * kT;
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = smem_desc(q_addr + blk * (kR * 128) + kk * 32, 16, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(st_addr + blk * (kT * 128) + kk * 32, 16, 1024, kSwizzle128B);
+                        mma_bf16(d_c, a, bd, id_s, (blk > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+#pragma unroll
+                for (int kk = 0; kk < kHalfRope / 16; ++kk) {
+                    const uint64_t a = smem_desc(q_addr + kQLat + kk * 32, 16, 512, kSwizzle64B);
+                    const uint64_t bd = smem_desc(st_addr + kSLat + kk * 32, 16, 512, kSwizzle64B);
+                    if (PLAIN)
+                        mma_bf16(d_c, a, bd, id_s, 1u);
+                    else
+                        mma_bf16(d_r, a, bd, id_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&sfull[s]);
+                if (j >= 1) ok = issue_o(j - 1);
+            }
+            if (ok && n_t > 0) ok = issue_o(n_t - 1);
+            if (!ok) *(volatile int*)abort_flag = 1;
+        }
+    } else {
+        // ===================== softmax / exchange / epilogue: thread = query row =====================
+        const int sub = warp & 3;                        // TMEM sub-partition = exchange slice
+        const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
+        const int r = 32 * sub + lane;                   // M=128 accumulator: row r in TMEM lane r
+        const int g = (r % p.H) / hpg;
+        const float coef = coef_s[r];
+        const float rs = p.scale * kLog2e;
+        const uint32_t my_slice = (uint32_t)sub * (kXB / 4);
+        const uint32_t peer_x = map_to_rank(smem_u32(sX) + my_slice, peer);
+        const uint32_t peer_xfull = map_to_rank(smem_u32(&xfull[sub]), peer);
+        const uint32_t peer_xfree = map_to_rank(smem_u32(&xfree[sub]), peer);
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_t; ++j) {
+            const int s = j & 1;
+            const int tile = jt0 + j;
+            bool got = wait_bounded(&sfull[s], (j >> 1) & 1, p.status);
+            tc_fence_after();
+            const float* ak_t = (const float*)(sm + kOffStage + s * kStageB + kSLat + kSRope);
+            float lg[kT];
+#pragma unroll
+            for (int c = 0; c < kT / 16; ++c) {
+                uint32_t sc[16], sr[16];
+                tmem_ld16(tmem + kCSc + s * kT + lane_base + 16 * c, sc);
+                if (!PLAIN) tmem_ld16(tmem + kCSr + s * kT + lane_base + 16 * c, sr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int t = 16 * c + jj;
+                    lg[t] = PLAIN ? rs * __uint_as_float(sc[jj])
+                                  : fmaf(coef * ak_t[t * p.G + g], __uint_as_float(sc[jj]), __uint_as_float(sr[jj]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sfree[s]);
+            // Y holds P of the previous tile until its output MMA is done
+            if (j >= 1) got = wait_bounded(odone, (j - 1) & 1, p.status) && got;
+#pragma unroll
+            for (int k = 0; k < kT / 4; ++k)
+                *reinterpret_cast<float4*>(sY + xoff(r, k)) = make_float4(lg[4 * k], lg[4 * k + 1], lg[4 * k + 2], lg[4 * k + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                // the other CTA's warp has consumed the previous tile from these rows
+                bool free_ok = (j == 0) || wait_bounded_cluster(&xfree[sub], (j - 1) & 1, p.status);
+                if (free_ok && got) {
+                    bulk_copy_to_cta(peer_x, sY + my_slice, kXB / 4, peer_xfull);
+                    bulk_commit_group();
+                } else {
+                    got = false;
+                }
+            }
+            got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+            const bool got_x = got && wait_bounded_cluster(&xfull[sub], j & 1, p.status);
+            if (got_x) {
+#pragma unroll
+                for (int k = 0; k < kT / 4; ++k) {
+                    const float4 v = *reinterpret_cast<const float4*>(sX + xoff(r, k));
+                    lg[4 * k] += v.x;
+                    lg[4 * k + 1] += v.y;
+                    lg[4 * k + 2] += v.z;
+                    lg[4 * k + 3] += v.w;
+                }
+            }
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, got_x)) { ok = false; *(volatile int*)abort_flag = 1; break; }
+            if (lane == 0 && j + 1 < n_t) {
+                mbar_arrive_expect_tx(&xfull[sub], kXB / 4);   // arm for the next tile, then release the rows
+                mbar_arrive_remote(peer_xfree);
+            }
+            const int valid = min(kT, L - tile * kT);
+            if (valid < kT) {
+#pragma unroll
+                for (int t = 0; t < kT; ++t)
+                    if (t >= valid) lg[t] = -INFINITY;
+            }
+            float mt = lg[0];
+#pragma unroll
+            for (int t = 1; t < kT; ++t) mt = fmaxf(mt, lg[t]);
+            // lazy running max: move it only when the tile max exceeds it by > 8 (log2);
+            // this row's O (its TMEM lane) is rescaled by this thread alone
+            float corr = 1.f;
+            const bool need = mt > m_run + 8.f;
+            if (need) {
+                corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mt);
+                m_run = mt;
+            }
+            // TMEM loads/stores are warp-collective: the whole warp rescales when any
+            // of its rows needs it, each lane by its own factor (1 for the others)
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int c16 = 0; c16 < kHalfLat; c16 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tmem + kCO + c16 + lane_base, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) * corr);
+                    tmem_st16(tmem + kCO + c16 + lane_base, v);
+                }
+                tmem_wait_st();
+            }
+            l_run *= corr;
+            // P row r into Y once the bulk copy has finished reading this warp's slice
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            float psum = 0.f;
+#pragma unroll
+            for (int k8 = 0; k8 < kT / 8; ++k8) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float e0 = fast_exp2(lg[8 * k8 + 2 * q] - m_run);
+                    const float e1 = fast_exp2(lg[8 * k8 + 2 * q + 1] - m_run);
+                    psum += e0 + e1;
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
+                    w4[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+                *reinterpret_cast<uint4*>(sY + poff(r, 8 * k8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            l_run += psum;
+            if (valid < kT) {   // zero this CTA's latent rows past the sequence end (this warp's share)
+                uint8_t* stg = sm + kOffStage + s * kStageB;
+                const int nrow = kT - valid;
+                for (int e = lane + 32 * sub; e < nrow * 4 * 8; e += 128) {
+                    const int rr = valid + e / 32, rem = e % 32;
+                    *reinterpret_cast<uint4*>(stg + (rem >> 3) * (kT * 128) + rr * 128 + (rem & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pfull[s]);
+        }
+        // ---- epilogue: thread = row, its 256 latents ----
+        bool got_last = (ok && n_t > 0) ? wait_bounded(odone, (n_t - 1) & 1, p.status) : true;
+        got_last = __all_sync(0xffffffffu, got_last);      // TMEM reads below are warp-collective
+        tc_fence_after();
+        if (!got_last) *(volatile int*)abort_flag = 1;
+        const size_t orow = ((size_t)b * p.s_q + qi) * p.H + r;
+        if (rank == 0) {
+            const float lse = (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+            if (it.part < 0) {
+                if (p.lse) p.lse[orow] = lse;
+            } else {
+                p.lse_part[(size_t)it.part * p.s_q * p.H + (size_t)qi * p.H + r] = lse;
+            }
+        }
+        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        float* dst_part = (it.part >= 0)
+                              ? p.o_part + ((size_t)it.part * p.s_q * p.H + (size_t)qi * p.H + r) * kDC + rank * kHalfLat
+                              : nullptr;
+#pragma unroll 1
+        for (int c16 = 0; c16 < kHalfLat; c16 += 16) {
+            uint32_t v[16];
+            if (n_t > 0 && got_last) {
+                tmem_ld16(tmem + kCO + c16 + lane_base, v);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) v[jj] = 0u;
+            }
+            float o16[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) o16[jj] = __uint_as_float(v[jj]) * inv;
+            if (dst_part) {
+                float4* d4 = reinterpret_cast<float4*>(dst_part + c16);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) d4[q] = make_float4(o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
+            } else if (p.o_dtype == QKMLA_F32) {
+                float4* d4 = reinterpret_cast<float4*>((float*)p.o + orow * kDC + rank * kHalfLat + c16);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) d4[q] = make_float4(o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
+            } else {
+                uint32_t w[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(o16[2 * q], o16[2 * q + 1]);
+                    w[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+                uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)p.o + orow * kDC + rank * kHalfLat + c16);
+                d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();            // no remote access to this CTA after this point
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+int launch_pair(const qkmla_decode_args* a, const TcParams& tp, int max_items, cudaStream_t s) {
+    CUtensorMap lat, rope;
+    const int row = a->d_c + a->d_r;
+    if (!make_map(&lat, a->kv_cache, a->num_slots, row, 64, kT, CU_TENSOR_MAP_SWIZZLE_128B)) return QKMLA_ERR_CUDA;
+    if (!make_map(&rope, a->kv_cache, a->num_slots, row, 32, kT, CU_TENSOR_MAP_SWIZZLE_64B)) return QKMLA_ERR_CUDA;
+    const bool plain = (a->flags & QKMLA_FLAG_PLAIN_MLA) != 0;
+    auto k = plain ? decode_pair_kernel<true> : decode_pair_kernel<false>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytesP) != cudaSuccess)
+        return QKMLA_ERR_CUDA;
+    dim3 grid(2 * a->s_q, max_items);
+    k<<<grid, kThreadsP, kBytesP, s>>>(lat, rope, tp);
+    return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
+}
+
+}  // namespace dec
+}  // namespace qkmla

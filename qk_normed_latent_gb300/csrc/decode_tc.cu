@@ -29,6 +29,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "decode_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace qkmla {
@@ -36,84 +37,11 @@ namespace qkmla {
 namespace {
 
 using namespace tc;
+using namespace dec;
 
 constexpr int kTile = 32;          // tokens per tile (a page holds a whole number of tiles)
 constexpr int kRowsMMA = 64;       // M of the logit MMA
 constexpr int kThreads = 192;
-constexpr int kMaxG = 8;
-constexpr int kMaxB = 4096;
-constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s bound on any single wait
-
-struct WorkItem {
-    int b;
-    int tile_begin;
-    int tile_end;
-    int part;          // -1: the item is the whole sequence, write the final row
-};
-
-struct TcParams {
-    const __nv_bfloat16* qt;   // [B][s_q][H][d_c]
-    const float* aq;           // [B][s_q][H]
-    const float* qr;           // [B][s_q][H][d_r]
-    const float* grq;          // [d_r] or null
-    const float* ak;           // [num_slots][G]
-    const int32_t* seq_lens;
-    const int32_t* page_table;
-    int64_t num_pages;
-    int page_size, max_pages;
-    int B, s_q, H, G;
-    int rows_o;                // query rows per CTA (N of the output MMA)
-    float scale, eps;
-    const WorkItem* items;
-    const int* n_items;
-    float* o_part;             // [max_items][s_q*H][d_c]
-    float* lse_part;           // [max_items][s_q*H]
-    void* o;
-    int o_dtype;
-    float* lse;
-    int* status;
-};
-
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded wait: spins on try_wait, checks the wall clock every 256 polls.
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && globaltimer() - t0 > kWaitNs) {
-            report(status, QKMLA_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ bool named_bar_any(int pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, 1, 128, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(pred)
-        : "memory");
-    return r != 0;
-}
-__device__ __forceinline__ void named_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b, float& ra, float& rb) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    ra = __low2float(v);
-    rb = __high2float(v);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
 // ---------------------------------------------------------------------------
 // shared-memory layout
 // ---------------------------------------------------------------------------
@@ -220,7 +148,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                 ss = fmaf(vals[j], vals[j], ss);
             }
             ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            const float beta = PLAIN ? 1.f : 1.f / sqrtf(ss / (float)DR + p.eps);
+            // QK mode: the RoPE query carries scale*log2e, so the MMA delivers the RoPE
+            // logit already in the exp2 domain
+            const float beta = PLAIN ? 1.f : p.scale * kLog2e / sqrtf(ss / (float)DR + p.eps);
             uint8_t* qrope = sQ + LY::kQLat;
 #pragma unroll
             for (int j = 0; j < DR / 2; j += 2) {
@@ -348,9 +278,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
         // ===================== softmax / rescale / epilogue =====================
         const int sub = warp & 3;                      // TMEM sub-partition of this warp
         const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
-        // M=64 accumulator layout: row r sits in lane r%16 of sub-partition r/16
-        const int r = 16 * sub + lane;
-        const bool row_ok = lane < 16 && r < rows_o;
+        // M=64 accumulator layout: row r sits in lane r%16 of sub-partition r/16.  The
+        // 16x32bx2 TMEM load gives lanes 0-15 tokens 0-15 and lanes 16-31 tokens 16-31
+        // of the same 16 rows: two threads per row, every lane busy.
+        const int half = lane >> 4;
+        const int r = 16 * sub + (lane & 15);
+        const int tb = 16 * half;                      // first token of this thread's half
+        const bool row_ok = r < rows_o;
         const int g = row_ok ? ((h0 + r) % p.H) / hpg : 0;
         const float coef = row_ok ? coef_s[r] : 0.f;
         const float rs = p.scale * kLog2e;
@@ -368,41 +302,39 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             uint8_t* stg = sm + LY::kOffStage + s * LY::kStage;
             const float* ak_t = (const float*)(stg + LY::kSLat + LY::kSRope);
             const int valid = min(kTile, L - tile * kTile);
-            float lg[kTile];
-            float mt = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kTile / 16; ++c) {
-                uint32_t sc[16], sr[16];
-                tmem_ld16(tmem + kColSc + sb * kTile + lane_base + 16 * c, sc);
-                if (!PLAIN) tmem_ld16(tmem + kColSr + sb * kTile + lane_base + 16 * c, sr);
-                tmem_wait_ld();
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int t = 16 * c + jj;
-                    float v;
-                    if (PLAIN) {
-                        v = rs * __uint_as_float(sc[jj]);
-                    } else {
-                        v = fmaf(coef * ak_t[t * p.G + g], __uint_as_float(sc[jj]), rs * __uint_as_float(sr[jj]));
-                    }
-                    v = (t < valid) ? v : -INFINITY;
-                    lg[t] = v;
-                    mt = fmaxf(mt, v);
-                }
-            }
+            uint32_t sc[16], sr[16];
+            tmem_ld16x2(tmem + kColSc + sb * kTile + lane_base, sc);
+            if (!PLAIN) tmem_ld16x2(tmem + kColSr + sb * kTile + lane_base, sr);
+            tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sfree[sb]);
+            float lg[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                if (PLAIN)
+                    lg[jj] = rs * __uint_as_float(sc[jj]);
+                else
+                    lg[jj] = fmaf(coef * ak_t[(tb + jj) * p.G + g], __uint_as_float(sc[jj]), __uint_as_float(sr[jj]));
+            }
+            if (valid < kTile) {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    if (tb + jj >= valid) lg[jj] = -INFINITY;
+            }
+            float mt = lg[0];
+#pragma unroll
+            for (int jj = 1; jj < 16; ++jj) mt = fmaxf(mt, lg[jj]);
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
             // lazy running max: move it only when the tile max exceeds it by > 8 (log2)
             float corr = 1.f;
             int need = 0;
             if (row_ok && mt > m_run + 8.f) {
-                const float mn = mt;
-                corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mn);
-                m_run = mn;
+                corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mt);
+                m_run = mt;
                 need = (j > 0) ? 1 : 0;
             }
-            if (lane < 16 && r < kRowsMMA) corr_s[r] = row_ok ? corr : 1.f;
+            if (half == 0) corr_s[r] = row_ok ? corr : 1.f;
             const bool any = named_bar_any(need || !got_s);
             if (any && *(volatile int*)abort_flag) { ok = false; break; }
             if (any) {
@@ -428,23 +360,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                 named_bar_sync();
             }
             l_run *= corr;
-            // P^T row r: 32 tokens (64 B) into the RoPE slot of this stage, 64-byte swizzle
+            // P^T row r, this thread's 16 tokens (32 B), 64-byte swizzle, into the RoPE slot
             uint8_t* pT = stg + LY::kSLat;
             float psum = 0.f;
+            uint32_t w8[8];
 #pragma unroll
-            for (int k8 = 0; k8 < kTile / 8; ++k8) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int t = 8 * k8 + 2 * q;
-                    const float e0 = (lg[t] == -INFINITY) ? 0.f : exp2f(lg[t] - m_run);
-                    const float e1 = (lg[t + 1] == -INFINITY) ? 0.f : exp2f(lg[t + 1] - m_run);
-                    float r0, r1;
-                    w4[q] = pack_bf16(e0, e1, r0, r1);
-                    psum += r0 + r1;
-                }
-                if (row_ok)
-                    *reinterpret_cast<uint4*>(pT + sw64_offset(r, 8 * k8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            for (int q = 0; q < 8; ++q) {
+                const float e0 = fast_exp2(lg[2 * q] - m_run);
+                const float e1 = fast_exp2(lg[2 * q + 1] - m_run);
+                psum += e0 + e1;
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
+                w8[q] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            if (row_ok) {
+                *reinterpret_cast<uint4*>(pT + sw64_offset(r, tb)) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+                *reinterpret_cast<uint4*>(pT + sw64_offset(r, tb + 8)) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
             }
             l_run += psum;
             // the last tile of the sequence: zero the latent rows past its end so that
@@ -464,12 +394,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(&pfull[s]);
         }
+        // the two halves of a row hold partial sums
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
         // ---- epilogue ----
         const bool got_last = (ok && n_t > 0) ? wait_bounded(odone, (n_t - 1) & 1, p.status) : true;
         if (named_bar_any(!got_last)) ok = false;
         tc_fence_after();
         if (!ok) *(volatile int*)abort_flag = 1;
-        if (row_ok) {
+        if (row_ok && half == 0) {
             l_s[r] = l_run;
             const float lse = (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
             const size_t orow = ((size_t)b * p.s_q + qi) * p.H + h0 + r;
@@ -511,6 +443,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             }
         }
     }
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -524,8 +457,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
 // scheduler: seq_lens -> work items (one CTA)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
-sched_kernel(const int32_t* __restrict__ seq_lens, int B, int s_q, int max_len, int n_rb, int sms, int min_tiles,
-             int fixed_splits, WorkItem* __restrict__ items, int* __restrict__ n_items, int* __restrict__ seq_nsplit,
+sched_kernel(const int32_t* __restrict__ seq_lens, int B, int s_q, int max_len, int n_rb, int sms, int min_tokens,
+             int tile, int fixed_splits, WorkItem* __restrict__ items, int* __restrict__ n_items, int* __restrict__ seq_nsplit,
              int* __restrict__ seq_part0, int* status) {
     __shared__ int tiles_s[kMaxB];
     __shared__ int ns_by_rank[kMaxB];
@@ -540,7 +473,7 @@ sched_kernel(const int32_t* __restrict__ seq_lens, int B, int s_q, int max_len, 
         if (L < s_q || L > max_len) {
             report(status, QKMLA_ERR_DEVICE_BOUNDS);
         } else {
-            tl = (L + kTile - 1) / kTile;
+            tl = (L + tile - 1) / tile;
         }
         tiles_s[b] = tl;
         tot += tl;
@@ -567,7 +500,7 @@ sched_kernel(const int32_t* __restrict__ seq_lens, int B, int s_q, int max_len, 
         // ideal tiles per CTA if the whole GPU shares the work evenly
         const float ideal = (float)s_total * n_rb / (float)sms;
         int tpi = (float)m <= 1.25f * ideal ? m : (int)ceilf(ideal);
-        s_tpi = max(max(tpi, min_tiles), 1);
+        s_tpi = max(max(tpi, min_tokens / tile), 1);
     }
     __syncthreads();
     const int tpi = s_tpi;
@@ -663,31 +596,6 @@ combine_var_kernel(const float* __restrict__ o_part, const float* __restrict__ l
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        cudaDriverEntryPointQueryResult q;
-        void* f = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess || q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
-    }
-    return fn;
-}
-
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int row_elems, int box_cols, CUtensorMapSwizzle sw) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
-    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kTile};
-    cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int DC, int DR, bool PLAIN, int NST>
 int launch_kernel(const CUtensorMap& lat, const CUtensorMap& rope, const TcParams& tp, int n_rb, int max_items,
                   cudaStream_t s) {
@@ -702,6 +610,40 @@ int launch_kernel(const CUtensorMap& lat, const CUtensorMap& rope, const TcParam
 }
 
 }  // namespace
+
+namespace dec {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int row_elems, int box_cols, int box_rows,
+              CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace dec
+
+// The two-CTA cluster kernel: DeepSeek-V3 decode shape, 128 heads per query token.
+bool pair_shape(const qkmla_decode_args* a) {
+    return a->d_c == 512 && a->d_r == 64 && a->H == 128 && a->page_size % 64 == 0;
+}
 
 // Shapes the tensor-core kernel is built for (bf16 cache).
 bool tc_supported(const qkmla_decode_args* a) {
@@ -752,16 +694,17 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     int* status = device_status_ptr();
     const int max_len = a->max_pages * a->page_size;
 
-    sched_kernel<<<1, 1024, 0, s>>>(a->seq_lens, a->B, a->s_q, max_len, n_rb, sms, /*min_tiles=*/16, a->num_splits,
-                                    items, n_items, seq_nsplit, seq_part0, status);
+    const int tile = pair_shape(a) ? 64 : kTile;
+    sched_kernel<<<1, 1024, 0, s>>>(a->seq_lens, a->B, a->s_q, max_len, n_rb, sms, /*min_tokens=*/512, tile,
+                                    a->num_splits, items, n_items, seq_nsplit, seq_part0, status);
     if (cudaGetLastError() != cudaSuccess) return QKMLA_ERR_CUDA;
 
     CUtensorMap lat, rope;
     const int row = a->d_c + a->d_r;
-    if (!make_map(&lat, a->kv_cache, a->num_slots, row, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return QKMLA_ERR_CUDA;
+    if (!make_map(&lat, a->kv_cache, a->num_slots, row, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B)) return QKMLA_ERR_CUDA;
     if (a->d_r == 64) {
         rope = lat;
-    } else if (!make_map(&rope, a->kv_cache, a->num_slots, row, 32, CU_TENSOR_MAP_SWIZZLE_64B)) {
+    } else if (!make_map(&rope, a->kv_cache, a->num_slots, row, 32, kTile, CU_TENSOR_MAP_SWIZZLE_64B)) {
         return QKMLA_ERR_CUDA;
     }
     TcParams tp;
@@ -789,7 +732,9 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     tp.status = status;
     const bool plain = (a->flags & QKMLA_FLAG_PLAIN_MLA) != 0;
     int rc;
-    if (a->d_c == 512) {
+    if (pair_shape(a)) {
+        rc = launch_pair(a, tp, max_items, s);
+    } else if (a->d_c == 512) {
         rc = plain ? launch_kernel<512, 64, true, 4>(lat, rope, tp, n_rb, max_items, s)
                    : launch_kernel<512, 64, false, 4>(lat, rope, tp, n_rb, max_items, s);
     } else {

@@ -83,12 +83,18 @@ def test_absorb_matches_oracle(Q, widx, qt, plain):
     ref_qt, ref_aq = O.absorb_query(q, gq, gk, wk, w.eps, plain=plain)
     np.testing.assert_allclose(_np(aq_out), ref_aq, rtol=2e-6)
     g = _np(qt_out)
+    # summation error of a length-d_h dot product is bounded relative to the sum
+    # of |terms| (not to |result|): scale_n = sum_j |W_nj q'_j|, computed in fp64
+    qa = np.abs(q.astype(np.float64)) * (1.0 if plain else np.abs(gq.astype(np.float64) * gk))
+    wa = np.abs(wk.astype(np.float64))
+    g_of = np.arange(w.H) // (w.H // w.G)
+    scale = np.stack([qa[:, h, :] @ wa[g_of[h]].T for h in range(w.H)], axis=1)
     if qt == "f32":
         assert np.max(np.abs(g - ref_qt)) <= 1e-5 * max(1.0, np.abs(ref_qt).max())
     else:
-        # one bf16 rounding of an fp32 value: within one bf16 ulp of the exact value
-        ulp = np.maximum(np.abs(ref_qt), 1e-30) * 2.0 ** -7
-        assert np.all(np.abs(g - ref_qt) <= ulp + 1e-6)
+        # one bf16 rounding (<= 2^-8 relative) on top of a GEMM accurate to 2^-15 of
+        # sum|terms| (split-bf16 tensor cores keep ~2^-17; fp32 FMA ~2^-20)
+        assert np.all(np.abs(g - ref_qt) <= 2.0 ** -8 * np.abs(ref_qt) + 2.0 ** -15 * scale)
 
 
 # ---------------------------------------------------------------------------
@@ -209,6 +215,28 @@ def test_tensor_core_kernel_is_selected_and_agrees_with_simt(Q, name):
     assert Q.get_device_status() == 0
     check_close(_np(st.o), o_s, "bf16", f"{name} tc-vs-simt o")
     check_close(_np(st.lse), l_s, "bf16", f"{name} tc-vs-simt lse")
+
+
+@pytest.mark.parametrize("name", ["dsv3_B4_T4096", "mixed_sq2_B3", "small_bf16_B3"])
+def test_plain_with_outliers_rescales_agree_across_kernels(Q, name):
+    """Plain MLA on x30-outlier data: unbounded logits make the running max move
+    on different tiles for different rows, exercising every rescale path of the
+    tensor-core kernel.  Both kernels see the same q~ and cache; they must agree
+    (bf16 P vs fp32 P: relative L2 within 1e-2)."""
+    from qk_normed_latent_gb300.pipeline import DeviceState
+    w = _workload(name)
+    st = DeviceState(w, plain=True)
+    st.absorb()
+    st.append_step()
+    for _ in range(3):                          # repeated launches on the same state
+        st.decode()
+    assert Q.get_device_status() == 0
+    o_tc, l_tc = _np(st.o).copy(), _np(st.lse).copy()
+    st.decode(force_simt=True)
+    o_s, l_s = _np(st.o), _np(st.lse)
+    assert np.all(np.isfinite(o_tc)) and np.all(np.isfinite(l_tc))
+    assert np.linalg.norm(o_tc - o_s) <= 1e-2 * np.linalg.norm(o_s)
+    assert np.max(np.abs(l_tc - l_s)) <= 1e-2 * max(1.0, np.abs(l_s).max())
 
 
 @pytest.mark.parametrize("splits", [1, 2, 5, 33])
