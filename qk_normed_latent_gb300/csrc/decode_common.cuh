@@ -165,6 +165,15 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
+// Relaxed remote arrive: only orders this thread's earlier READS of the rows the
+// other CTA will overwrite (their values are already consumed), no release fence.
+// `dep` is a value computed from every read that must complete first; taking it
+// as an operand makes the instruction wait for those reads.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar, float dep) {
+    asm volatile("{\n\t.reg .f32 d;\n\tmov.f32 d, %1;\n\t"
+                 "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n\t}"
+                 ::"r"(remote_bar), "f"(dep) : "memory");
+}
 // Pull a 2-D tensor-map box into L2 ahead of its TMA load.
 __device__ __forceinline__ void tma_prefetch_l2(const void* tmap, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"

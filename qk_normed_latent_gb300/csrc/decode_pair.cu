@@ -21,7 +21,8 @@
 //     shared memory (completing on a per-warp mbarrier there), then adds the
 //     rows it received -- fp32 addition commutes, so both CTAs hold
 //     bit-identical logits and P,
-//   * accumulates O = P C over its 256 latents (M=128 rows, N=256, K=64).
+//   * writes P (bf16) into TMEM and accumulates O = P C over its 256 latents
+//     (M=128 rows, N=256, K=64 tokens, A read from TMEM).
 // Each CTA streams only its half of every tile from HBM.
 //
 // Warps: 0 TMA producer (+ TMEM owner), 1 MMA issuer, 2-5 softmax / exchange /
@@ -62,8 +63,9 @@ constexpr int kBytesP = kOffMisc + kNumBars * 8 + 16 + kR * 4 + 1024;
 static_assert(kStageB % 1024 == 0 && kOffStage % 1024 == 0 && kOffX % 1024 == 0 && kOffY % 1024 == 0, "align");
 static_assert(kBytesP <= 232448, "shared memory budget");
 
-// TMEM columns: S_c[2] at 0/64, S_r[2] at 128/192, O (128 rows x 256 latents) at 256
-constexpr uint32_t kCSc = 0, kCSr = 128, kCO = 256;
+// TMEM columns: S_c at 0, S_r at 64, P[2] (64 bf16 tokens = 32 columns each) at
+// 128 / 160, O (128 rows x 256 latents) at 256
+constexpr uint32_t kCSc = 0, kCSr = 64, kCP = 128, kCO = 256;
 
 // Byte offset of floats 4k..4k+3 of row r in an exchange buffer: rows of 256 B,
 // 16-byte chunks XOR-swizzled; rows 32w..32w+31 form warp w's 8 KB slice.
@@ -86,8 +88,9 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     uint64_t* bars = (uint64_t*)(sm + kOffMisc);
     uint64_t* full = bars;          // [2] TMA -> MMA
     uint64_t* empty = bars + 2;     // [2] output MMA done -> TMA
-    uint64_t* sfull = bars + 4;     // [2] logit MMA done -> softmax
-    uint64_t* sfree = bars + 6;     // [2] softmax read S -> MMA
+    uint64_t* sfull = bars + 4;     // logit MMA done -> softmax (one S buffer)
+    uint64_t* sfree = bars + 5;     // softmax read S -> MMA
+    uint64_t* pdone = bars + 6;     // [2] output MMA done with P buffer -> softmax
     uint64_t* pfull = bars + 8;     // [2] P written -> output MMA
     uint64_t* odone = bars + 10;    // output MMA of a tile done
     uint64_t* xfull = bars + 11;    // [4] per warp: the other CTA's partial rows landed in X
@@ -114,7 +117,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     if (tid == 0) {
         if (bad && rank == 0) report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
         for (int i = 0; i < kNumBars; ++i) {
-            const bool four = (i == 6 || i == 7 || i == 8 || i == 9);   // sfree, pfull: one per softmax warp
+            const bool four = (i == 5 || i == 8 || i == 9);   // sfree, pfull: one per softmax warp
             mbar_init(&bars[i], four ? 4u : 1u);
         }
         *abort_flag = 0;
@@ -207,7 +210,6 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             const uint32_t id_s = idesc_bf16(kR, kT, 0, 0);
             const uint32_t id_o = idesc_bf16(kR, kHalfLat, 0, 1);
             const uint32_t q_addr = smem_u32(sQ);
-            const uint32_t y_addr = smem_u32(sY);
             auto issue_o = [&](int jj) -> bool {
                 const int s = jj & 1;
                 if (!wait_bounded(&pfull[s], (jj >> 1) & 1, p.status)) return false;
@@ -215,13 +217,14 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 const uint32_t st_addr = smem_u32(sm + kOffStage + s * kStageB);
 #pragma unroll
                 for (int kk = 0; kk < kT / 16; ++kk) {
-                    // A = P: K-major, 8-row groups 2048 B apart; B = C^T: this CTA's 256
-                    // latents (4 boxes, LBO = box stride) x 16 tokens (8-token groups, SBO)
-                    const uint64_t a = smem_desc(y_addr + kk * 32, 16, 2048, kSwizzle128B);
+                    // A = P from TMEM (16 tokens = 8 packed columns per step); B = C^T: this
+                    // CTA's 256 latents (4 boxes, LBO = box stride) x 16 tokens (SBO = 8 tokens)
                     const uint64_t bd = smem_desc(st_addr + kk * 2048, kT * 128, 1024, kSwizzle128B);
-                    mma_bf16(tmem + kCO, a, bd, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16_tmem_a(tmem + kCO, tmem + kCP + s * (kT / 2) + kk * 8, bd, id_o,
+                                    (jj > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(&empty[s]);
+                mma_commit(&pdone[s]);
                 mma_commit(odone);
                 return true;
             };
@@ -229,18 +232,17 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             for (int j = 0; j < n_t && ok; ++j) {
                 const int s = j & 1;
                 if (!wait_bounded(&full[s], (j >> 1) & 1, p.status)) { ok = false; break; }
-                if (j >= 2 && !wait_bounded(&sfree[s], ((j >> 1) - 1) & 1, p.status)) { ok = false; break; }
+                // single S buffer: the softmax has read the previous tile's logits
+                if (j >= 1 && !wait_bounded(sfree, (j - 1) & 1, p.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t st_addr = smem_u32(sm + kOffStage + s * kStageB);
-                const uint32_t d_c = tmem + kCSc + s * kT;
-                const uint32_t d_r = tmem + kCSr + s * kT;
 #pragma unroll
                 for (int blk = 0; blk < 4; ++blk) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t a = smem_desc(q_addr + blk * (kR * 128) + kk * 32, 16, 1024, kSwizzle128B);
                         const uint64_t bd = smem_desc(st_addr + blk * (kT * 128) + kk * 32, 16, 1024, kSwizzle128B);
-                        mma_bf16(d_c, a, bd, id_s, (blk > 0 || kk > 0) ? 1u : 0u);
+                        mma_bf16(tmem + kCSc, a, bd, id_s, (blk > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
 #pragma unroll
@@ -248,11 +250,11 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                     const uint64_t a = smem_desc(q_addr + kQLat + kk * 32, 16, 512, kSwizzle64B);
                     const uint64_t bd = smem_desc(st_addr + kSLat + kk * 32, 16, 512, kSwizzle64B);
                     if (PLAIN)
-                        mma_bf16(d_c, a, bd, id_s, 1u);
+                        mma_bf16(tmem + kCSc, a, bd, id_s, 1u);
                     else
-                        mma_bf16(d_r, a, bd, id_s, kk > 0 ? 1u : 0u);
+                        mma_bf16(tmem + kCSr, a, bd, id_s, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&sfull[s]);
+                mma_commit(sfull);
                 if (j >= 1) ok = issue_o(j - 1);
             }
             if (ok && n_t > 0) ok = issue_o(n_t - 1);
@@ -272,31 +274,39 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
         const uint32_t peer_xfree = map_to_rank(smem_u32(&xfree[sub]), peer);
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_t; ++j) {
-            const int s = j & 1;
-            const int tile = jt0 + j;
-            bool got = wait_bounded(&sfull[s], (j >> 1) & 1, p.status);
+        // partial logits of one tile (this CTA's half of K), scaled: S from TMEM
+        auto partial = [&](int j, float (&out)[kT]) -> bool {
+            const bool got = wait_bounded(sfull, j & 1, p.status);
             tc_fence_after();
-            const float* ak_t = (const float*)(sm + kOffStage + s * kStageB + kSLat + kSRope);
-            float lg[kT];
+            const float* ak_t = (const float*)(sm + kOffStage + (j & 1) * kStageB + kSLat + kSRope);
 #pragma unroll
-            for (int c = 0; c < kT / 16; ++c) {
-                uint32_t sc[16], sr[16];
-                tmem_ld16(tmem + kCSc + s * kT + lane_base + 16 * c, sc);
-                if (!PLAIN) tmem_ld16(tmem + kCSr + s * kT + lane_base + 16 * c, sr);
+            for (int c = 0; c < kT / 32; ++c) {
+                uint32_t sc[32], sr[32];
+                tmem_ld16(tmem + kCSc + lane_base + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(sc));
+                tmem_ld16(tmem + kCSc + lane_base + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
+                if (!PLAIN) {
+                    tmem_ld16(tmem + kCSr + lane_base + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(sr));
+                    tmem_ld16(tmem + kCSr + lane_base + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(sr + 16));
+                }
                 tmem_wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int t = 16 * c + jj;
-                    lg[t] = PLAIN ? rs * __uint_as_float(sc[jj])
-                                  : fmaf(coef * ak_t[t * p.G + g], __uint_as_float(sc[jj]), __uint_as_float(sr[jj]));
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int t = 32 * c + jj;
+                    out[t] = PLAIN ? rs * __uint_as_float(sc[jj])
+                                   : fmaf(coef * ak_t[t * p.G + g], __uint_as_float(sc[jj]), __uint_as_float(sr[jj]));
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sfree[s]);
-            // Y holds P of the previous tile until its output MMA is done
-            if (j >= 1) got = wait_bounded(odone, (j - 1) & 1, p.status) && got;
+            if (lane == 0) mbar_arrive(sfree);
+            return got;
+        };
+        float lg[kT];
+        for (int j = 0; j < n_t; ++j) {
+            const int s = j & 1;
+            const int tile = jt0 + j;
+            bool got = partial(j, lg);
+            // stage this tile's partial rows and send them to the other CTA
 #pragma unroll
             for (int k = 0; k < kT / 4; ++k)
                 *reinterpret_cast<float4*>(sY + xoff(r, k)) = make_float4(lg[4 * k], lg[4 * k + 1], lg[4 * k + 2], lg[4 * k + 3]);
@@ -304,7 +314,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             __syncwarp();
             if (lane == 0) {
                 // the other CTA's warp has consumed the previous tile from these rows
-                bool free_ok = (j == 0) || wait_bounded_cluster(&xfree[sub], (j - 1) & 1, p.status);
+                const bool free_ok = (j == 0) || wait_bounded_cluster(&xfree[sub], (j - 1) & 1, p.status);
                 if (free_ok && got) {
                     bulk_copy_to_cta(peer_x, sY + my_slice, kXB / 4, peer_xfull);
                     bulk_commit_group();
@@ -324,23 +334,28 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                     lg[4 * k + 3] += v.w;
                 }
             }
-            __syncwarp();
             if (!__all_sync(0xffffffffu, got_x)) { ok = false; *(volatile int*)abort_flag = 1; break; }
-            if (lane == 0 && j + 1 < n_t) {
-                mbar_arrive_expect_tx(&xfull[sub], kXB / 4);   // arm for the next tile, then release the rows
-                mbar_arrive_remote(peer_xfree);
-            }
             const int valid = min(kT, L - tile * kT);
             if (valid < kT) {
 #pragma unroll
                 for (int t = 0; t < kT; ++t)
                     if (t >= valid) lg[t] = -INFINITY;
             }
-            float mt = lg[0];
+            float mx[8];                                   // tree max: short dependency chains
 #pragma unroll
-            for (int t = 1; t < kT; ++t) mt = fmaxf(mt, lg[t]);
-            // lazy running max: move it only when the tile max exceeds it by > 8 (log2);
-            // this row's O (its TMEM lane) is rescaled by this thread alone
+            for (int q = 0; q < 8; ++q) mx[q] = fmaxf(fmaxf(lg[q], lg[q + 8]), fmaxf(lg[q + 16], lg[q + 24]));
+#pragma unroll
+            for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], fmaxf(fmaxf(lg[q + 32], lg[q + 40]), fmaxf(lg[q + 48], lg[q + 56])));
+            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            // every X value has been read (mt depends on all of them): arm for the next
+            // tile and let the other CTA overwrite these rows
+            const float mt_w = warp_max(mt);
+            if (lane == 0 && j + 1 < n_t) {
+                mbar_arrive_expect_tx(&xfull[sub], kXB / 4);
+                mbar_arrive_remote_relaxed(peer_xfree, mt_w);
+            }
+            // lazy running max: move it only when the tile max exceeds it by > 8 (log2)
             float corr = 1.f;
             const bool need = mt > m_run + 8.f;
             if (need) {
@@ -350,6 +365,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             // TMEM loads/stores are warp-collective: the whole warp rescales when any
             // of its rows needs it, each lane by its own factor (1 for the others)
             if (j > 0 && __any_sync(0xffffffffu, need)) {
+                const bool got_o = wait_bounded(odone, (j - 1) & 1, p.status);
+                if (!__all_sync(0xffffffffu, got_o)) { ok = false; *(volatile int*)abort_flag = 1; break; }
                 tc_fence_after();
 #pragma unroll 1
                 for (int c16 = 0; c16 < kHalfLat; c16 += 16) {
@@ -363,24 +380,28 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 tmem_wait_st();
             }
             l_run *= corr;
-            // P row r into Y once the bulk copy has finished reading this warp's slice
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
-            float psum = 0.f;
-#pragma unroll
-            for (int k8 = 0; k8 < kT / 8; ++k8) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float e0 = fast_exp2(lg[8 * k8 + 2 * q] - m_run);
-                    const float e1 = fast_exp2(lg[8 * k8 + 2 * q + 1] - m_run);
-                    psum += e0 + e1;
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
-                    w4[q] = *reinterpret_cast<const uint32_t*>(&b2);
-                }
-                *reinterpret_cast<uint4*>(sY + poff(r, 8 * k8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            // P (bf16) into TMEM buffer s once the output MMA two tiles back released it
+            if (j >= 2) {
+                const bool got_p = wait_bounded(&pdone[s], ((j >> 1) - 1) & 1, p.status);
+                if (!__all_sync(0xffffffffu, got_p)) { ok = false; *(volatile int*)abort_flag = 1; break; }
+                tc_fence_after();
             }
-            l_run += psum;
+            float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t w16[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float e0 = fast_exp2(lg[32 * h + 2 * q] - m_run);
+                    const float e1 = fast_exp2(lg[32 * h + 2 * q + 1] - m_run);
+                    ps4[q & 3] += e0 + e1;
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
+                    w16[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+                tmem_st16(tmem + kCP + s * (kT / 2) + 16 * h + lane_base, w16);
+            }
+            tmem_wait_st();
+            l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
             if (valid < kT) {   // zero this CTA's latent rows past the sequence end (this warp's share)
                 uint8_t* stg = sm + kOffStage + s * kStageB;
                 const int nrow = kT - valid;
@@ -389,11 +410,15 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                     *reinterpret_cast<uint4*>(stg + (rem >> 3) * (kT * 128) + rr * 128 + (rem & 7) * 16) =
                         make_uint4(0, 0, 0, 0);
                 }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&pfull[s]);
+            if (lane == 0) {
+                mbar_arrive(&pfull[s]);
+                bulk_wait_read_all();       // Y may be restaged for the next tile
+            }
+            __syncwarp();
         }
         // ---- epilogue: thread = row, its 256 latents ----
         bool got_last = (ok && n_t > 0) ? wait_bounded(odone, (n_t - 1) & 1, p.status) : true;
