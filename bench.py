@@ -142,13 +142,18 @@ def traffic_from_profiles(kernel_sig: str):
     return None
 
 
+DECODE_SOURCES = ("common.cuh", "tc_ptx.cuh", "decode_common.cuh", "decode_tc.cu", "decode_pair.cu",
+                  "decode_simt.cu")
+
+
 def kernel_signature():
+    """Hash of the sources the decode kernels are compiled from: a traffic
+    figure recorded under another hash belongs to a kernel that has changed."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "qk_normed_latent_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in DECODE_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -267,7 +272,7 @@ def main():
     if Q.get_device_status() != 0:
         raise RuntimeError("device status error during warm-up")
     kernel = Q.decode_kernel_name(st.args)
-    launches_per_step = 1 + (1 if st.c_new is not None else 0) + 1 + (1 if Q.decode_workspace_size(st.args) else 0)
+    launches_per_step = 1 + (1 if st.c_new is not None else 0) + Q.decode_launch_count(st.args)
 
     def timed_steps(state, K):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),

@@ -194,6 +194,14 @@ int qkmla_version(void);
 const char* qkmla_decode_kernel_name(const qkmla_decode_args* a);
 
 /*
+ * qkmla_decode_launch_count -- number of kernels one qkmla_decode call with
+ * these arguments launches on the stream (tensor-core path: split scheduler,
+ * decode, combine; CUDA-core path: decode, plus combine when it splits).
+ * Returns 0 for arguments qkmla_decode would reject.
+ */
+int qkmla_decode_launch_count(const qkmla_decode_args* a);
+
+/*
  * qkmla_decode_noalloc -- qkmla_decode for callers that cannot allocate
  * device memory when they decode: a runtime that hands out only pre-planned
  * buffers, a plugin whose host owns every allocation, or a thread that must

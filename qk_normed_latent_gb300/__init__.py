@@ -22,6 +22,7 @@ FLAG_FORCE_SIMT = 2
 SYMBOLS = [
     "qkmla_absorb_query", "qkmla_append", "qkmla_decode_workspace_size", "qkmla_decode",
     "qkmla_get_device_status", "qkmla_status_string", "qkmla_version", "qkmla_decode_kernel_name",
+    "qkmla_decode_launch_count",
 ]
 
 
@@ -91,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.qkmla_version.restype = i
         L.qkmla_decode_kernel_name.argtypes = [ctypes.POINTER(DecodeArgs)]
         L.qkmla_decode_kernel_name.restype = ctypes.c_char_p
+        L.qkmla_decode_launch_count.argtypes = [ctypes.POINTER(DecodeArgs)]
+        L.qkmla_decode_launch_count.restype = i
         if hasattr(L, "qkmla_decode_noalloc"):
             L.qkmla_decode_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), vp]
             L.qkmla_decode_noalloc.restype = i
@@ -198,6 +201,10 @@ def decode_workspace_size(args: DecodeArgs) -> int:
 
 def decode_kernel_name(args: DecodeArgs) -> str:
     return lib().qkmla_decode_kernel_name(ctypes.byref(args)).decode()
+
+
+def decode_launch_count(args: DecodeArgs) -> int:
+    return int(lib().qkmla_decode_launch_count(ctypes.byref(args)))
 
 
 def decode_raw(args: DecodeArgs, stream=None) -> None:

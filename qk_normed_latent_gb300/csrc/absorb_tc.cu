@@ -10,8 +10,13 @@
 // and W_g [d_c, d_h] (both K-major, fp32).  To keep fp32-level accuracy on the
 // bf16 tensor cores every operand is split into x = hi + lo (two bf16 values,
 // lo = bf16(x - hi)) and three MMAs accumulate hi*hi + hi*lo + lo*hi in fp32
-// (the dropped lo*lo term is ~2^-16 relative).  A CTA owns 128 rows of one
-// group and all d_c outputs; the accumulator sits in TMEM (up to 512 columns).
+// (the dropped lo*lo term is ~2^-16 relative).
+//
+// A CTA owns a 128-row x 256-latent output tile of one group.  Its raw fp32
+// operands land in shared memory by bulk copies (one per query row, eight for
+// the W_g slice), all in flight at once; the 512 threads then split them into
+// bf16 hi/lo in place (each thread reads its elements, a barrier, then writes
+// the swizzled K-major tiles over the raw bytes: 4 bytes in, 2 x 2 bytes out).
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -22,8 +27,8 @@ namespace {
 using namespace tc;
 
 constexpr int kM = 128;          // rows per CTA (MMA M)
-constexpr int kN = 256;          // MMA N per chunk
-constexpr int kThreads = 128;
+constexpr int kN = 256;          // latent columns per CTA (MMA N)
+constexpr int kThreads = 512;
 
 __device__ __forceinline__ void split_store(uint8_t* hi_base, uint8_t* lo_base, uint32_t off, const float (&x)[8]) {
     uint32_t h[4], l[4];
@@ -40,16 +45,23 @@ __device__ __forceinline__ void split_store(uint8_t* hi_base, uint8_t* lo_base, 
     *reinterpret_cast<uint4*>(lo_base + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// Shared memory: A_hi, A_lo [kM x DH] and B_hi, B_lo [kN x DH], bf16, K-major,
-// 128-byte swizzle, in 64-column blocks.
+// Shared memory.  A region: raw fp32 [kM][DH], then A_hi, A_lo (bf16 [kM x DH],
+// K-major, 128-byte swizzle, 64-column blocks) over the same bytes; B region
+// likewise for [kN][DH].  Thread t handles the 8-element groups
+// e = t + i * kThreads (row e / kG8, columns 8 (e % kG8) .. +7).
 template <int DH>
 struct AbsLayout {
-    static constexpr int kKBlocks = DH / 64;
-    static constexpr int kA = kKBlocks * kM * 128;
-    static constexpr int kB = kKBlocks * kN * 128;
-    static constexpr int kOffAhi = 0, kOffAlo = kA, kOffBhi = 2 * kA, kOffBlo = 2 * kA + kB;
-    static constexpr int kOffMisc = 2 * kA + 2 * kB;
+    static constexpr int kA = kM * DH * 4;                    // raw A bytes = A_hi + A_lo bytes
+    static constexpr int kB = kN * DH * 4;
+    static constexpr int kOffA = 0, kOffB = kA;
+    static constexpr int kOffAlo = kA / 2, kOffBlo = kOffB + kB / 2;
+    static constexpr int kOffG = kA + kB;                     // gamma_q * gamma_k [DH]
+    static constexpr int kOffMisc = kOffG + DH * 4;
     static constexpr int kBytes = kOffMisc + 64 + 1024;
+    static constexpr int kG8 = DH / 8;
+    static constexpr int kAIter = kM * kG8 / kThreads;
+    static constexpr int kBIter = kN * kG8 / kThreads;
+    static constexpr int kBCopies = 8;
 };
 
 template <int DH, typename OutT>
@@ -58,147 +70,177 @@ absorb_tc_kernel(const float* __restrict__ q, const float* __restrict__ gq, cons
                  const float* __restrict__ wk, int rows, int H, int G, int d_c, float eps, int plain,
                  OutT* __restrict__ qt, float* __restrict__ aq, int* status) {
     using LY = AbsLayout<DH>;
+    static_assert(LY::kAIter * kThreads == kM * LY::kG8 && LY::kBIter * kThreads == kN * LY::kG8, "tiling");
+    static_assert(32 % LY::kG8 == 0, "a row's groups sit in one warp");
+    static_assert(LY::kB % (LY::kBCopies * 16) == 0, "bulk copy sizes");
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    float* rawA = reinterpret_cast<float*>(sm + LY::kOffA);
+    float* rawB = reinterpret_cast<float*>(sm + LY::kOffB);
+    float* gprod = reinterpret_cast<float*>(sm + LY::kOffG);
     uint64_t* bar = (uint64_t*)(sm + LY::kOffMisc);
-    uint32_t* tmem_slot = (uint32_t*)(bar + 1);
+    uint32_t* tmem_slot = (uint32_t*)(bar + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = blockIdx.y;
+    const int g = blockIdx.z;
+    const int n0 = blockIdx.y * kN;
     const int hpg = H / G;
     const int M = rows * hpg;
     const int m0 = blockIdx.x * kM;
-    const int n_chunks = d_c / kN;
+    const int m_valid = min(kM, M - m0);
 
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
         fence_barrier_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 512);
+        tmem_alloc(tmem_slot, kN);
         tmem_relinquish();
     }
-    // ---- A = q * gamma_q * gamma_k (or q), split hi/lo ----
-    for (int e = tid; e < kM * (DH / 8); e += kThreads) {
-        const int ml = e / (DH / 8), k8 = e % (DH / 8);
-        const int m = m0 + ml;
-        float x[8];
-        if (m < M) {
-            const int r = m / hpg, h = g * hpg + m % hpg;
-            const float4* src = reinterpret_cast<const float4*>(q + ((size_t)r * H + h) * DH + k8 * 8);
-            const float4 v0 = src[0], v1 = src[1];
-            x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
-            x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
-            if (!plain) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] *= gq[k8 * 8 + i] * gk[k8 * 8 + i];
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = 0.f;
-        }
-        const uint32_t off = (k8 >> 3) * (kM * 128) + sw128_offset(ml, (k8 & 7) * 8);
-        split_store(sm + LY::kOffAhi, sm + LY::kOffAlo, off, x);
+    __syncthreads();
+    // ---- every operand byte in flight at once ----
+    if (tid == 0) mbar_arrive_expect_tx(&bar[0], (uint32_t)(m_valid * DH * 4 + LY::kB));
+    if (tid < m_valid) {
+        const int m = m0 + tid, r = m / hpg, h = g * hpg + m % hpg;
+        bulk_load(rawA + tid * DH, q + ((size_t)r * H + h) * DH, DH * 4, &bar[0]);
+    } else if (tid >= kM && tid < kM + LY::kBCopies) {
+        const int c = tid - kM;
+        constexpr int bytes = LY::kB / LY::kBCopies;
+        bulk_load(reinterpret_cast<uint8_t*>(rawB) + c * bytes,
+                  reinterpret_cast<const uint8_t*>(wk + ((size_t)g * d_c + n0) * DH) + c * bytes, bytes, &bar[0]);
     }
-    // alpha^q: one thread per row from the raw query
+    if (tid < DH) gprod[tid] = plain ? 1.f : gq[tid] * gk[tid];
+    bool ok = mbar_wait(&bar[0], 0, 1u << 24);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) report(status, QKMLA_ERR_TIMEOUT);
+        // copies that never landed may still be in flight: do not release the CTA's memory early
+        mbar_wait(&bar[0], 0, 1u << 24);
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(*tmem_slot, kN);
+        return;
+    }
+
+    // ---- A = q * gamma_q * gamma_k (or q), split hi/lo in place; alpha^q from the raw q ----
     {
-        const int m = m0 + tid;
-        if (tid < kM && m < M) {
-            const int r = m / hpg, h = g * hpg + m % hpg;
-            const float4* src = reinterpret_cast<const float4*>(q + ((size_t)r * H + h) * DH);
-            float ss = 0.f;
-#pragma unroll 4
-            for (int k4 = 0; k4 < DH / 4; ++k4) {
-                const float4 v = src[k4];
-                ss = fmaf(v.x, v.x, ss);
-                ss = fmaf(v.y, v.y, ss);
-                ss = fmaf(v.z, v.z, ss);
-                ss = fmaf(v.w, v.w, ss);
+        float x[LY::kAIter][8];
+#pragma unroll
+        for (int i = 0; i < LY::kAIter; ++i) {
+            const int e = tid + i * kThreads;
+            const int ml = e / LY::kG8, k8 = e % LY::kG8;
+            if (ml < m_valid) {
+                const float4 v0 = *reinterpret_cast<const float4*>(rawA + ml * DH + k8 * 8);
+                const float4 v1 = *reinterpret_cast<const float4*>(rawA + ml * DH + k8 * 8 + 4);
+                x[i][0] = v0.x; x[i][1] = v0.y; x[i][2] = v0.z; x[i][3] = v0.w;
+                x[i][4] = v1.x; x[i][5] = v1.y; x[i][6] = v1.z; x[i][7] = v1.w;
+            } else {
+#pragma unroll
+                for (int t = 0; t < 8; ++t) x[i][t] = 0.f;
             }
-            aq[(size_t)r * H + h] = plain ? 1.f : 1.f / sqrtf(ss / (float)DH + eps);
+            if (blockIdx.y == 0) {
+                // the kG8 groups of one row are held by kG8 consecutive lanes
+                float ss = 0.f;
+#pragma unroll
+                for (int t = 0; t < 8; ++t) ss = fmaf(x[i][t], x[i][t], ss);
+#pragma unroll
+                for (int o = LY::kG8 / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                if (k8 == 0 && ml < m_valid) {
+                    const int m = m0 + ml, r = m / hpg, h = g * hpg + m % hpg;
+                    aq[(size_t)r * H + h] = plain ? 1.f : 1.f / sqrtf(ss / (float)DH + eps);
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) x[i][t] *= gprod[k8 * 8 + t];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < LY::kAIter; ++i) {
+            const int e = tid + i * kThreads;
+            const int ml = e / LY::kG8, k8 = e % LY::kG8;
+            const uint32_t off = (k8 >> 3) * (kM * 128) + sw128_offset(ml, (k8 & 7) * 8);
+            split_store(sm + LY::kOffA, sm + LY::kOffAlo, off, x[i]);
         }
     }
+    // ---- B = W_g rows n0 .. n0 + 255, split hi/lo in place ----
+    {
+        float x[LY::kBIter][8];
+#pragma unroll
+        for (int i = 0; i < LY::kBIter; ++i) {
+            const int e = tid + i * kThreads;
+            const int nl = e / LY::kG8, k8 = e % LY::kG8;
+            const float4 v0 = *reinterpret_cast<const float4*>(rawB + nl * DH + k8 * 8);
+            const float4 v1 = *reinterpret_cast<const float4*>(rawB + nl * DH + k8 * 8 + 4);
+            x[i][0] = v0.x; x[i][1] = v0.y; x[i][2] = v0.z; x[i][3] = v0.w;
+            x[i][4] = v1.x; x[i][5] = v1.y; x[i][6] = v1.z; x[i][7] = v1.w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < LY::kBIter; ++i) {
+            const int e = tid + i * kThreads;
+            const int nl = e / LY::kG8, k8 = e % LY::kG8;
+            const uint32_t off = (k8 >> 3) * (kN * 128) + sw128_offset(nl, (k8 & 7) * 8);
+            split_store(sm + LY::kOffB, sm + LY::kOffBlo, off, x[i]);
+        }
+    }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const float* wg = wk + (size_t)g * d_c * DH;
-    bool ok = true;
-
-    for (int nc = 0; nc < n_chunks; ++nc) {
-        // ---- B = W_g rows nc*256 .. +255, split hi/lo ----
-        for (int e = tid; e < kN * (DH / 8); e += kThreads) {
-            const int nl = e / (DH / 8), k8 = e % (DH / 8);
-            const float4* src = reinterpret_cast<const float4*>(wg + (size_t)(nc * kN + nl) * DH + k8 * 8);
-            const float4 v0 = src[0], v1 = src[1];
-            float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-            const uint32_t off = (k8 >> 3) * (kN * 128) + sw128_offset(nl, (k8 & 7) * 8);
-            split_store(sm + LY::kOffBhi, sm + LY::kOffBlo, off, x);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-            const uint32_t idesc = idesc_bf16(kM, kN, 0, 0);
-            const uint32_t a_hi = smem_u32(sm + LY::kOffAhi), a_lo = smem_u32(sm + LY::kOffAlo);
-            const uint32_t b_hi = smem_u32(sm + LY::kOffBhi), b_lo = smem_u32(sm + LY::kOffBlo);
-            const uint32_t d = tmem + nc * kN;
+    if (tid == 0) {
+        const uint32_t idesc = idesc_bf16(kM, kN, 0, 0);
+        const uint32_t a_hi = smem_u32(sm + LY::kOffA), a_lo = smem_u32(sm + LY::kOffAlo);
+        const uint32_t b_hi = smem_u32(sm + LY::kOffB), b_lo = smem_u32(sm + LY::kOffBlo);
 #pragma unroll
-            for (int kb = 0; kb < DH / 16; ++kb) {
-                const uint32_t ao = (kb >> 2) * (kM * 128) + (kb & 3) * 32;
-                const uint32_t bo = (kb >> 2) * (kN * 128) + (kb & 3) * 32;
-                mma_bf16(d, smem_desc(a_hi + ao, 16, 1024, kSwizzle128B), smem_desc(b_hi + bo, 16, 1024, kSwizzle128B),
-                         idesc, kb > 0 ? 1u : 0u);
-                mma_bf16(d, smem_desc(a_hi + ao, 16, 1024, kSwizzle128B), smem_desc(b_lo + bo, 16, 1024, kSwizzle128B),
-                         idesc, 1u);
-                mma_bf16(d, smem_desc(a_lo + ao, 16, 1024, kSwizzle128B), smem_desc(b_hi + bo, 16, 1024, kSwizzle128B),
-                         idesc, 1u);
-            }
-            mma_commit(bar);
+        for (int kb = 0; kb < DH / 16; ++kb) {
+            const uint32_t ao = (kb >> 2) * (kM * 128) + (kb & 3) * 32;
+            const uint32_t bo = (kb >> 2) * (kN * 128) + (kb & 3) * 32;
+            mma_bf16(tmem, smem_desc(a_hi + ao, 16, 1024, kSwizzle128B), smem_desc(b_hi + bo, 16, 1024, kSwizzle128B),
+                     idesc, kb > 0 ? 1u : 0u);
+            mma_bf16(tmem, smem_desc(a_hi + ao, 16, 1024, kSwizzle128B), smem_desc(b_lo + bo, 16, 1024, kSwizzle128B),
+                     idesc, 1u);
+            mma_bf16(tmem, smem_desc(a_lo + ao, 16, 1024, kSwizzle128B), smem_desc(b_hi + bo, 16, 1024, kSwizzle128B),
+                     idesc, 1u);
         }
-        __syncwarp();
-        // every thread waits (bounded) before B is overwritten or TMEM is read
-        uint32_t done = 0;
-        for (uint32_t it = 0; it < (1u << 24) && !done; ++it) done = mbar_try_wait(bar, nc & 1) ? 1u : 0u;
-        if (!done) {
-            report(status, QKMLA_ERR_TIMEOUT);
-            ok = false;
-        }
-        tc_fence_after();
-        if (__syncthreads_or(!ok)) break;
+        mma_commit(&bar[1]);
     }
+    __syncwarp();
+    // every thread waits (bounded) before TMEM is read
+    ok = mbar_wait(&bar[1], 0, 1u << 24);
+    if (!ok) report(status, QKMLA_ERR_TIMEOUT);
+    tc_fence_after();
 
-    // ---- epilogue: row m = lane 32*warp + lane; columns = latent coordinates ----
-    if (ok) {
-        const int m = m0 + 32 * warp + lane;
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        const bool valid = m < M;
-        OutT* dst = nullptr;
-        if (valid) {
-            const int r = m / hpg, h = g * hpg + m % hpg;
-            dst = qt + ((size_t)r * H + h) * d_c;
-        }
-        for (int c0 = 0; c0 < d_c; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(tmem + lane_base + c0, v);
-            tmem_wait_ld();
-            if (valid) {
+    // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (output rows) and
+    //      columns 64 (w / 4) .. +63 (latent coordinates n0 + ...) ----
+    if (__all_sync(0xffffffffu, ok)) {
+        const int ml = 32 * (warp & 3) + lane;
+        const int c_base = 64 * (warp >> 2);
+        const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + c_base;
+        uint32_t v[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld16(taddr + 16 * c, v[c]);
+        tmem_wait_ld();
+        if (ml < m_valid) {
+            const int m = m0 + ml, r = m / hpg, h = g * hpg + m % hpg;
+            OutT* dst = qt + ((size_t)r * H + h) * d_c + n0 + c_base;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
                 if constexpr (sizeof(OutT) == 2) {
                     uint32_t w[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                        const __nv_bfloat162 b2 =
+                            __floats2bfloat162_rn(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1]));
                         w[i] = *reinterpret_cast<const uint32_t*>(&b2);
                     }
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * c);
                     d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
                     d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
                 } else {
-                    float4* d4 = reinterpret_cast<float4*>(dst + c0);
+                    float4* d4 = reinterpret_cast<float4*>(dst + 16 * c);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                            __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                        d4[i] = make_float4(__uint_as_float(v[c][4 * i]), __uint_as_float(v[c][4 * i + 1]),
+                                            __uint_as_float(v[c][4 * i + 2]), __uint_as_float(v[c][4 * i + 3]));
                 }
             }
         }
@@ -208,7 +250,7 @@ absorb_tc_kernel(const float* __restrict__ q, const float* __restrict__ gq, cons
     if (warp == 0) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, kN);
     }
 }
 
@@ -221,7 +263,7 @@ int launch_t(const float* q, const float* gq, const float* gk, const float* wk, 
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes) != cudaSuccess)
         return QKMLA_ERR_CUDA;
     const int M = rows * (H / G);
-    dim3 grid((M + kM - 1) / kM, G);
+    dim3 grid((M + kM - 1) / kM, d_c / kN, G);
     k<<<grid, kThreads, LY::kBytes, s>>>(q, gq, gk, wk, rows, H, G, d_c, eps, plain ? 1 : 0, (OutT*)qt, aq,
                                          device_status_ptr());
     return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
@@ -229,11 +271,11 @@ int launch_t(const float* q, const float* gq, const float* gk, const float* wk, 
 
 }  // namespace
 
-// Shapes the tensor-core absorb handles: d_h in {64, 128}, d_c a multiple of 256
-// up to 512, 16-byte aligned fp32 inputs.
+// Shapes the tensor-core absorb handles: d_h in {64, 128}, d_c a multiple of
+// 256, 16-byte aligned fp32 inputs.
 bool absorb_tc_supported(const float* q, const float* wk, int d_h, int d_c) {
     if (d_h != 64 && d_h != 128) return false;
-    if (d_c % kN || d_c > 512) return false;
+    if (d_c % kN) return false;
     if (((uintptr_t)q % 16) || ((uintptr_t)wk % 16)) return false;
     return true;
 }

@@ -159,6 +159,13 @@ const char* qkmla_decode_kernel_name(const qkmla_decode_args* a) {
     return plan.kernel == 1 ? "tcgen05" : "simt";
 }
 
+int qkmla_decode_launch_count(const qkmla_decode_args* a) {
+    DecodePlan plan;
+    if (plan_decode(a, &plan) != QKMLA_OK) return 0;
+    if (plan.kernel == 1) return 3;
+    return plan.parts > 1 ? 2 : 1;
+}
+
 int qkmla_decode(const qkmla_decode_args* a, void* stream) {
     DecodePlan plan;
     const int rc = plan_decode(a, &plan);

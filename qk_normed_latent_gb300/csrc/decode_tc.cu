@@ -578,17 +578,38 @@ combine_var_kernel(const float* __restrict__ o_part, const float* __restrict__ l
     }
     __syncthreads();
     const float inv = s_inv;
-    for (int k = tid; k < d_c; k += 128) {
-        float acc = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            const float w = w_s[s];
-            if (w != 0.f) acc = fmaf(w, o_part[((size_t)(p0 + s) * rows_per_seq + rr) * d_c + k], acc);
+    // float4 columns; eight splits' loads are in flight before any is summed
+    for (int k4 = tid; k4 < d_c / 4; k4 += 128) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < ns; s0 += 8) {
+            float4 v[8];
+            float wv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int sp = s0 + u;
+                wv[u] = sp < ns ? w_s[sp] : 0.f;
+                v[u] = wv[u] != 0.f
+                           ? reinterpret_cast<const float4*>(o_part + ((size_t)(p0 + sp) * rows_per_seq + rr) * d_c)[k4]
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                acc.x = fmaf(wv[u], v[u].x, acc.x);
+                acc.y = fmaf(wv[u], v[u].y, acc.y);
+                acc.z = fmaf(wv[u], v[u].z, acc.z);
+                acc.w = fmaf(wv[u], v[u].w, acc.w);
+            }
         }
-        acc *= inv;
-        if (o_dtype == QKMLA_F32)
-            ((float*)o)[(size_t)row * d_c + k] = acc;
-        else
-            ((__nv_bfloat16*)o)[(size_t)row * d_c + k] = __float2bfloat16_rn(acc);
+        acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+        if (o_dtype == QKMLA_F32) {
+            reinterpret_cast<float4*>((float*)o + (size_t)row * d_c)[k4] = acc;
+        } else {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+            reinterpret_cast<uint2*>((__nv_bfloat16*)o + (size_t)row * d_c)[k4] = pk;
+        }
     }
     if (tid == 0 && lse) lse[row] = s_lse;
 }
@@ -654,7 +675,7 @@ bool tc_supported(const qkmla_decode_args* a) {
     const int rows_o = a->H < 64 ? a->H : 64;
     if (rows_o % 16 || a->H % rows_o) return false;
     if (rows_o > a->d_r) return false;     // P^T (rows_o x 32 tokens) reuses the tile's RoPE slot
-    if (((uintptr_t)a->kv_cache % 16) || ((uintptr_t)a->q_tilde % 16)) return false;
+    if (((uintptr_t)a->kv_cache % 16) || ((uintptr_t)a->q_tilde % 16) || ((uintptr_t)a->o % 16)) return false;
     if (!(a->flags & QKMLA_FLAG_PLAIN_MLA) && ((uintptr_t)a->ak_cache % 16)) return false;
     return true;
 }

@@ -146,6 +146,31 @@ def test_append_matches_oracle_bit_exact_layout(Q, cache, plain, widx):
     assert torch.equal(ak.cpu()[untouched].view(torch.int32), ak0.cpu()[untouched].view(torch.int32))
 
 
+@pytest.mark.parametrize("widx", [1, 2])
+def test_append_bulk_and_plain_kernels_agree(Q, widx):
+    """A misaligned token buffer sends qkmla_append to its plain-load kernel.  The
+    cache rows are pure casts and must match bit for bit; both kernels form each
+    key element with the same fp32 FMA chain but reduce the sum of squares over
+    the d_h elements in another order, so alpha^k agrees to fp32 rounding."""
+    w = W.WORKLOADS[widx]
+    wk, _, _, _, grk = W.weights(w)
+    c, r = W.sequence(W.small(w, 1, (77,)), 0)
+    slots = torch.arange(77, dtype=torch.int64, device="cuda") * 3
+    outs = []
+    for shift in (0, 1):
+        buf = torch.zeros(77 * w.d_c + 1, dtype=torch.float32, device="cuda")
+        cn = buf[shift:shift + 77 * w.d_c].view(77, w.d_c)
+        cn.copy_(torch.from_numpy(c))
+        kv = torch.zeros((256, w.d_c + w.d_r), dtype=torch.bfloat16, device="cuda")
+        ak = torch.zeros((256, w.G), dtype=torch.float32, device="cuda")
+        Q.append(cn, torch.from_numpy(r).cuda(), torch.from_numpy(wk).cuda(), torch.from_numpy(grk).cuda(),
+                 slots, kv, ak, w.eps)
+        assert Q.get_device_status() == 0
+        outs.append((kv.view(torch.int16).cpu(), ak.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0])
+    np.testing.assert_allclose(outs[0][1].numpy(), outs[1][1].numpy(), rtol=2e-6)
+
+
 def test_append_out_of_range_slot_is_reported(Q):
     w = W.WORKLOADS[1]
     wk = torch.from_numpy(W.weights(w)[0]).cuda()
