@@ -92,7 +92,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     uint64_t* sfree = bars + 5;     // softmax read S -> MMA
     uint64_t* pdone = bars + 6;     // [2] output MMA done with P buffer -> softmax
     uint64_t* pfull = bars + 8;     // [2] P written -> output MMA
-    uint64_t* odone = bars + 10;    // output MMA of a tile done
+    // bars + 10: spare
     uint64_t* xfull = bars + 11;    // [4] per warp: the other CTA's partial rows landed in X
     uint64_t* xfree = bars + 15;    // [4] per warp: the other CTA's X rows may be overwritten
     uint32_t* tmem_slot = (uint32_t*)(bars + kNumBars);
@@ -225,7 +225,6 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 }
                 mma_commit(&empty[s]);
                 mma_commit(&pdone[s]);
-                mma_commit(odone);
                 return true;
             };
             bool ok = true;
@@ -365,7 +364,9 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             // TMEM loads/stores are warp-collective: the whole warp rescales when any
             // of its rows needs it, each lane by its own factor (1 for the others)
             if (j > 0 && __any_sync(0xffffffffu, need)) {
-                const bool got_o = wait_bounded(odone, (j - 1) & 1, p.status);
+                // the previous tile's output MMA: its P buffer's barrier, whose earlier
+                // phases this warp has consumed (so the parity names one phase)
+                const bool got_o = wait_bounded(&pdone[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status);
                 if (!__all_sync(0xffffffffu, got_o)) { ok = false; *(volatile int*)abort_flag = 1; break; }
                 tc_fence_after();
 #pragma unroll 1
@@ -421,7 +422,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             __syncwarp();
         }
         // ---- epilogue: thread = row, its 256 latents ----
-        bool got_last = (ok && n_t > 0) ? wait_bounded(odone, (n_t - 1) & 1, p.status) : true;
+        bool got_last =
+            (ok && n_t > 0) ? wait_bounded(&pdone[(n_t - 1) & 1], ((n_t - 1) >> 1) & 1, p.status) : true;
         got_last = __all_sync(0xffffffffu, got_last);      // TMEM reads below are warp-collective
         tc_fence_after();
         if (!got_last) *(volatile int*)abort_flag = 1;

@@ -39,52 +39,77 @@ namespace {
 using namespace tc;
 using namespace dec;
 
-constexpr int kTile = 32;          // tokens per tile (a page holds a whole number of tiles)
 constexpr int kRowsMMA = 64;       // M of the logit MMA
 constexpr int kThreads = 192;
+
+// Tokens per tile: 128 for d_c = 256 (the logit MMA count per tile does not grow
+// with N up to 128, so wide tiles cut the MMA cost per token fourfold), 32 for
+// d_c = 512 (its Q tile and stages leave no room for wider ones).  A tile is
+// loaded in boxes of at most 64 tokens, each mapped through the page table.
+template <int DC>
+constexpr int tile_of() { return DC == 256 ? 128 : 32; }
+
 // ---------------------------------------------------------------------------
 // shared-memory layout
 // ---------------------------------------------------------------------------
-template <int DC, int DR, int NST>
+template <int DC, int DR, int NST, int KT>
 struct Layout {
-    static constexpr int kLatBlocks = DC / 64;                     // 64-column TMA boxes
-    static constexpr int kRopeRowBytes = DR * 2;                   // 128 (SW128) or 64 (SW64)
+    static constexpr int kBox = KT < 64 ? KT : 64;                  // tokens per TMA box
+    static constexpr int kSub = KT / kBox;                          // boxes per tile
+    static constexpr int kLatBlocks = DC / 64;                      // 64-column TMA boxes
+    static constexpr int kRopeRowBytes = DR * 2;                    // 128 (SW128) or 64 (SW64)
     static constexpr int kQLat = kLatBlocks * kRowsMMA * 128;
     static constexpr int kQRope = kRowsMMA * kRopeRowBytes;
-    static constexpr int kSLat = kLatBlocks * kTile * 128;
-    static constexpr int kSRope = kTile * kRopeRowBytes;
-    static constexpr int kSAk = kTile * kMaxG * 4;
+    static constexpr int kSLat = kLatBlocks * KT * 128;
+    static constexpr int kSRope = KT * kRopeRowBytes;
+    static constexpr int kSAk = KT * kMaxG * 4;
     static constexpr int kStage = ((kSLat + kSRope + kSAk) + 1023) / 1024 * 1024;
     static constexpr int kQ = ((kQLat + kQRope) + 1023) / 1024 * 1024;
     static constexpr int kOffQ = 0;
     static constexpr int kOffStage = kQ;
     static constexpr int kOffMisc = kQ + NST * kStage;
+    // logit buffers in TMEM: two when they fit beside the widest O^T (4 x 64 columns)
+    static constexpr int kChunks = DC / 128;
+    static constexpr int kNSB = (4 * KT + kChunks * 64 <= 512) ? 2 : 1;
+    static constexpr uint32_t kColSc = 0, kColSr = kNSB * KT, kColO = 2 * kNSB * KT;
     // misc: barriers then per-row arrays
-    static constexpr int kNumBars = 3 * NST + 5;
+    static constexpr int kNumBars = 3 * NST + 2 * kNSB + 1;
     static constexpr int kMisc = kNumBars * 8 + 16 + 4 * kRowsMMA * 4;
     static constexpr int kBytes = kOffMisc + kMisc + 1024;        // + alignment slack
-    static constexpr uint32_t kStageTx = (uint32_t)(kSLat + kSRope);
+    // bytes one box brings: latent blocks + RoPE rows (alpha^k is added at run time)
+    static constexpr uint32_t kBoxTx = (uint32_t)(kLatBlocks * kBox * 128 + kBox * kRopeRowBytes);
+    static_assert(kColO + kChunks * 64 <= 512, "TMEM budget");
+    static_assert(KT % 32 == 0 && KT <= 128, "tile");
 };
 
-// TMEM columns: S_c[2] at 0/32, S_r[2] at 64/96, O^T chunks from 256.
-constexpr uint32_t kColSc = 0, kColSr = 64, kColO = 256, kTmemCols = 512;
+constexpr uint32_t kTmemCols = 512;
 
-template <int DC, int DR, bool PLAIN, int NST>
+// Byte offset of P^T element (row r, token t) in the tile's RoPE slot: K-major
+// (K = tokens); 32-token tiles use 64-byte rows with the 64-byte swizzle, wider
+// tiles 64-token atoms of 128-byte rows with the 128-byte swizzle.
+template <int KT>
+__device__ __forceinline__ uint32_t pt_offset(int r, int t, int rows_o) {
+    if (KT == 32) return sw64_offset(r, t);
+    return (uint32_t)(t >> 6) * (uint32_t)(rows_o * 128) + sw128_offset(r, t & 63);
+}
+
+template <int DC, int DR, bool PLAIN, int NST, int KT>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
                  const TcParams p) {
-    using LY = Layout<DC, DR, NST>;
-    constexpr int kChunks = DC / 128;
+    using LY = Layout<DC, DR, NST, KT>;
+    constexpr int kChunks = LY::kChunks;
+    constexpr int NSB = LY::kNSB;
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     uint8_t* sQ = sm + LY::kOffQ;
     uint64_t* bars = (uint64_t*)(sm + LY::kOffMisc);
-    uint64_t* full = bars;                 // [NST] TMA -> MMA
-    uint64_t* empty = bars + NST;          // [NST] output MMA done -> TMA
-    uint64_t* pfull = bars + 2 * NST;      // [NST] P written -> output MMA
-    uint64_t* sfull = bars + 3 * NST;      // [2]  logit MMA done -> softmax
-    uint64_t* sfree = bars + 3 * NST + 2;  // [2]  softmax read S -> MMA
-    uint64_t* odone = bars + 3 * NST + 4;  // output MMA of a tile done
+    uint64_t* full = bars;                   // [NST] TMA -> MMA
+    uint64_t* empty = bars + NST;            // [NST] output MMA done -> TMA
+    uint64_t* pfull = bars + 2 * NST;        // [NST] P written -> output MMA
+    uint64_t* sfull = bars + 3 * NST;        // [NSB] logit MMA done -> softmax
+    uint64_t* sfree = sfull + NSB;           // [NSB] softmax read S -> MMA
+    uint64_t* odone = sfree + NSB;           // output MMA of a tile done
     uint32_t* tmem_slot = (uint32_t*)(bars + LY::kNumBars);
     int* abort_flag = (int*)(tmem_slot + 1);
     float* coef_s = (float*)(sm + LY::kOffMisc + LY::kNumBars * 8 + 16);
@@ -102,7 +127,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
     const int seq_len = p.seq_lens[b];
     const bool bad = seq_len < p.s_q || seq_len > p.max_pages * p.page_size;
     const int L = bad ? 0 : seq_len - p.s_q + qi + 1;
-    const int tiles = (L + kTile - 1) / kTile;
+    const int tiles = (L + KT - 1) / KT;
     const int jt0 = it.tile_begin;
     const int jt1 = min(it.tile_end, tiles);
     const int n_t = max(0, jt1 - jt0);
@@ -112,8 +137,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
         if (bad) report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
         for (int s = 0; s < LY::kNumBars; ++s) {
             uint32_t cnt = 1;
-            if (s >= 2 * NST && s < 3 * NST) cnt = 4;          // pfull: one arrive per softmax warp
-            if (s == 3 * NST + 2 || s == 3 * NST + 3) cnt = 4; // sfree
+            if (s >= 2 * NST && s < 3 * NST) cnt = 4;                  // pfull: one arrive per softmax warp
+            if (s >= 3 * NST + NSB && s < 3 * NST + 2 * NSB) cnt = 4;  // sfree
             mbar_init(&bars[s], cnt);
         }
         *abort_flag = 0;
@@ -183,33 +208,41 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                     break;
                 }
                 if (*(volatile int*)abort_flag) break;
-                const int t0 = (jt0 + j) * kTile;
-                const int pg = t0 / p.page_size;
-                int64_t page = p.page_table ? (int64_t)p.page_table[(int64_t)b * p.max_pages + pg]
-                                            : (int64_t)b * p.max_pages + pg;
-                if (page < 0 || page >= p.num_pages) {
-                    report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
-                    page = 0;
-                }
-                const int64_t slot0 = page * p.page_size + (t0 % p.page_size);
+                const int t0 = (jt0 + j) * KT;
+                // boxes wholly past the end of the sequence are not loaded
+                const int n_sub = min(LY::kSub, (L - t0 + LY::kBox - 1) / LY::kBox);
                 uint8_t* stg = sm + LY::kOffStage + s * LY::kStage;
-                mbar_arrive_expect_tx(&full[s], LY::kStageTx + (PLAIN ? 0u : (uint32_t)(kTile * p.G * 4)));
+                const uint32_t ak_bytes = PLAIN ? 0u : (uint32_t)(LY::kBox * p.G * 4);
+                mbar_arrive_expect_tx(&full[s], (uint32_t)n_sub * (LY::kBoxTx + ak_bytes));
+                for (int h = 0; h < n_sub; ++h) {
+                    const int tb = t0 + h * LY::kBox;
+                    const int pg = tb / p.page_size;
+                    int64_t page = p.page_table ? (int64_t)p.page_table[(int64_t)b * p.max_pages + pg]
+                                                : (int64_t)b * p.max_pages + pg;
+                    if (page < 0 || page >= p.num_pages) {
+                        report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
+                        page = 0;
+                    }
+                    const int64_t slot0 = page * p.page_size + (tb % p.page_size);
 #pragma unroll
-                for (int blk = 0; blk < LY::kLatBlocks; ++blk)
-                    tma_load_2d(stg + blk * (kTile * 128), &tm_lat, blk * 64, (int)slot0, &full[s]);
-                if (DR == 64)
-                    tma_load_2d(stg + LY::kSLat, &tm_lat, DC, (int)slot0, &full[s]);
-                else
-                    tma_load_2d(stg + LY::kSLat, &tm_rope, DC, (int)slot0, &full[s]);
-                if (!PLAIN)
-                    bulk_load(stg + LY::kSLat + LY::kSRope, p.ak + slot0 * p.G, (uint32_t)(kTile * p.G * 4),
-                              &full[s]);
+                    for (int blk = 0; blk < LY::kLatBlocks; ++blk)
+                        tma_load_2d(stg + blk * (KT * 128) + h * (LY::kBox * 128), &tm_lat, blk * 64, (int)slot0,
+                                    &full[s]);
+                    uint8_t* rope_dst = stg + LY::kSLat + h * (LY::kBox * LY::kRopeRowBytes);
+                    if (DR == 64)
+                        tma_load_2d(rope_dst, &tm_lat, DC, (int)slot0, &full[s]);
+                    else
+                        tma_load_2d(rope_dst, &tm_rope, DC, (int)slot0, &full[s]);
+                    if (!PLAIN)
+                        bulk_load(stg + LY::kSLat + LY::kSRope + h * (LY::kBox * p.G * 4), p.ak + slot0 * p.G,
+                                  ak_bytes, &full[s]);
+                }
             }
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
         if (lane == 0) {
-            const uint32_t id_s = idesc_bf16(kRowsMMA, kTile, 0, 0);
+            const uint32_t id_s = idesc_bf16(kRowsMMA, KT, 0, 0);
             const uint32_t id_o = idesc_bf16(128, rows_o, 1, 0);
             const uint32_t q_addr = smem_u32(sQ);
             auto issue_o = [&](int jj) -> bool {
@@ -221,13 +254,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                    for (int kk = 0; kk < KT / 16; ++kk) {
                         // A = C^T chunk c: MN-major, two 64-column boxes (LBO = box stride),
                         // 8-token groups 1024 B apart (SBO); B = P^T rows, K-major.
-                        const uint64_t a = smem_desc(st_addr + (2 * c) * (kTile * 128) + kk * 2048,
-                                                     kTile * 128, 1024, kSwizzle128B);
-                        const uint64_t bdesc = smem_desc(p_addr + kk * 32, 16, 512, kSwizzle64B);
-                        mma_bf16(tmem + kColO + c * rows_o, a, bdesc, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                        const uint64_t a = smem_desc(st_addr + (2 * c) * (KT * 128) + kk * 2048, KT * 128, 1024,
+                                                     kSwizzle128B);
+                        const uint64_t bdesc =
+                            KT == 32 ? smem_desc(p_addr + kk * 32, 16, 512, kSwizzle64B)
+                                     : smem_desc(p_addr + (kk >> 2) * (rows_o * 128) + (kk & 3) * 32, 16, 1024,
+                                                 kSwizzle128B);
+                        mma_bf16(tmem + LY::kColO + c * rows_o, a, bdesc, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
                 mma_commit(&empty[s]);
@@ -236,19 +272,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             };
             bool ok = true;
             for (int j = 0; j < n_t && ok; ++j) {
-                const int s = j % NST, sb = j & 1;
+                const int s = j % NST, sb = j % NSB;
                 if (!wait_bounded(&full[s], (j / NST) & 1, p.status)) { ok = false; break; }
-                if (j >= 2 && !wait_bounded(&sfree[sb], ((j >> 1) - 1) & 1, p.status)) { ok = false; break; }
+                if (j >= NSB && !wait_bounded(&sfree[sb], ((j / NSB) - 1) & 1, p.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t st_addr = smem_u32(sm + LY::kOffStage + s * LY::kStage);
-                const uint32_t d_c = tmem + kColSc + sb * kTile;
-                const uint32_t d_r = tmem + kColSr + sb * kTile;
+                const uint32_t d_c = tmem + LY::kColSc + sb * KT;
+                const uint32_t d_r = tmem + LY::kColSr + sb * KT;
 #pragma unroll
                 for (int blk = 0; blk < LY::kLatBlocks; ++blk) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t a = smem_desc(q_addr + blk * (kRowsMMA * 128) + kk * 32, 16, 1024, kSwizzle128B);
-                        const uint64_t bd = smem_desc(st_addr + blk * (kTile * 128) + kk * 32, 16, 1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(st_addr + blk * (KT * 128) + kk * 32, 16, 1024, kSwizzle128B);
                         mma_bf16(d_c, a, bd, id_s, (blk > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
@@ -279,52 +315,57 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
         const int sub = warp & 3;                      // TMEM sub-partition of this warp
         const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
         // M=64 accumulator layout: row r sits in lane r%16 of sub-partition r/16.  The
-        // 16x32bx2 TMEM load gives lanes 0-15 tokens 0-15 and lanes 16-31 tokens 16-31
-        // of the same 16 rows: two threads per row, every lane busy.
+        // 16x32bx2 TMEM load gives lanes 0-15 columns c..c+15 and lanes 16-31 columns
+        // c+16..c+31 of the same 16 rows: two threads per row, every lane busy.  A
+        // thread holds tokens 32 q + 16 half + (0..15) for q < KT/32.
+        constexpr int kQ4 = KT / 32;
         const int half = lane >> 4;
         const int r = 16 * sub + (lane & 15);
-        const int tb = 16 * half;                      // first token of this thread's half
+        const int tb = 16 * half;
         const bool row_ok = r < rows_o;
         const int g = row_ok ? ((h0 + r) % p.H) / hpg : 0;
         const float coef = row_ok ? coef_s[r] : 0.f;
         const float rs = p.scale * kLog2e;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
+        bool late_fail = false;      // a timed-out wait at the end of the previous tile
         for (int j = 0; j < n_t; ++j) {
-            const int s = j % NST, sb = j & 1;
+            const int s = j % NST, sb = j % NSB;
             const int tile = jt0 + j;
             // a timed-out wait is folded into the per-tile vote below, so every abort
             // decision is uniform across the four softmax warps (none is left at a
             // named barrier)
-            const bool got_s = wait_bounded(&sfull[sb], (j >> 1) & 1, p.status);
+            const bool got_s = wait_bounded(&sfull[sb], (j / NSB) & 1, p.status);
             if (!got_s) *(volatile int*)abort_flag = 1;
             tc_fence_after();
             uint8_t* stg = sm + LY::kOffStage + s * LY::kStage;
             const float* ak_t = (const float*)(stg + LY::kSLat + LY::kSRope);
-            const int valid = min(kTile, L - tile * kTile);
-            uint32_t sc[16], sr[16];
-            tmem_ld16x2(tmem + kColSc + sb * kTile + lane_base, sc);
-            if (!PLAIN) tmem_ld16x2(tmem + kColSr + sb * kTile + lane_base, sr);
-            tmem_wait_ld();
+            const int valid = min(KT, L - tile * KT);
+            float lg[kQ4][16];
+#pragma unroll
+            for (int q = 0; q < kQ4; ++q) {
+                uint32_t sc[16], sr[16];
+                tmem_ld16x2(tmem + LY::kColSc + sb * KT + 32 * q + lane_base, sc);
+                if (!PLAIN) tmem_ld16x2(tmem + LY::kColSr + sb * KT + 32 * q + lane_base, sr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int t = 32 * q + tb + jj;
+                    if (PLAIN)
+                        lg[q][jj] = rs * __uint_as_float(sc[jj]);
+                    else
+                        lg[q][jj] = fmaf(coef * ak_t[t * p.G + g], __uint_as_float(sc[jj]), __uint_as_float(sr[jj]));
+                    if (t >= valid) lg[q][jj] = -INFINITY;
+                }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sfree[sb]);
-            float lg[16];
+            float mt = -INFINITY;
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-                if (PLAIN)
-                    lg[jj] = rs * __uint_as_float(sc[jj]);
-                else
-                    lg[jj] = fmaf(coef * ak_t[(tb + jj) * p.G + g], __uint_as_float(sc[jj]), __uint_as_float(sr[jj]));
-            }
-            if (valid < kTile) {
+            for (int q = 0; q < kQ4; ++q)
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
-                    if (tb + jj >= valid) lg[jj] = -INFINITY;
-            }
-            float mt = lg[0];
-#pragma unroll
-            for (int jj = 1; jj < 16; ++jj) mt = fmaxf(mt, lg[jj]);
+                for (int jj = 0; jj < 16; ++jj) mt = fmaxf(mt, lg[q][jj]);
             mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
             // lazy running max: move it only when the tile max exceeds it by > 8 (log2)
             float corr = 1.f;
@@ -335,18 +376,23 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                 need = (j > 0) ? 1 : 0;
             }
             if (half == 0) corr_s[r] = row_ok ? corr : 1.f;
-            const bool any = named_bar_any(need || !got_s);
+            const bool any = named_bar_any(need || !got_s || late_fail);
             if (any && *(volatile int*)abort_flag) { ok = false; break; }
+            // odone completes once per tile.  Its phase j-1 (output MMA of the previous
+            // tile) is consumed on every tile, before P(j) is released: the barrier is
+            // then never two phases ahead of this wait, so the parity names one phase.
+            bool o_seen = (j == 0);
             if (any) {
                 // rescale O^T columns (rows) in TMEM once the previous output MMA is done
                 const bool got_o = wait_bounded(odone, (j - 1) & 1, p.status);
                 if (named_bar_any(!got_o)) { ok = false; break; }
+                o_seen = true;
                 tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < kChunks; ++c) {
                     for (int c16 = 0; c16 < rows_o; c16 += 16) {
                         uint32_t v[16];
-                        const uint32_t ta = tmem + kColO + c * rows_o + c16 + lane_base;
+                        const uint32_t ta = tmem + LY::kColO + c * rows_o + c16 + lane_base;
                         tmem_ld16(ta, v);
                         tmem_wait_ld();
 #pragma unroll
@@ -360,34 +406,43 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                 named_bar_sync();
             }
             l_run *= corr;
-            // P^T row r, this thread's 16 tokens (32 B), 64-byte swizzle, into the RoPE slot
+            // P^T row r, this thread's tokens, into the RoPE slot (bf16)
             uint8_t* pT = stg + LY::kSLat;
             float psum = 0.f;
-            uint32_t w8[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float e0 = fast_exp2(lg[2 * q] - m_run);
-                const float e1 = fast_exp2(lg[2 * q + 1] - m_run);
-                psum += e0 + e1;
-                const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
-                w8[q] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-            if (row_ok) {
-                *reinterpret_cast<uint4*>(pT + sw64_offset(r, tb)) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
-                *reinterpret_cast<uint4*>(pT + sw64_offset(r, tb + 8)) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+            for (int q = 0; q < kQ4; ++q) {
+                uint32_t w8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float e0 = fast_exp2(lg[q][2 * u] - m_run);
+                    const float e1 = fast_exp2(lg[q][2 * u + 1] - m_run);
+                    psum += e0 + e1;
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
+                    w8[u] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+                if (row_ok) {
+                    const int t = 32 * q + tb;
+                    *reinterpret_cast<uint4*>(pT + pt_offset<KT>(r, t, rows_o)) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+                    *reinterpret_cast<uint4*>(pT + pt_offset<KT>(r, t + 8, rows_o)) =
+                        make_uint4(w8[4], w8[5], w8[6], w8[7]);
+                }
             }
             l_run += psum;
             // the last tile of the sequence: zero the latent rows past its end so that
             // stale slot contents (possibly NaN) cannot reach the output MMA
-            if (valid < kTile) {
+            if (valid < KT) {
                 const int st = tid - 64;
-                const int nrow = kTile - valid;
+                const int nrow = KT - valid;
                 for (int e = st; e < nrow * LY::kLatBlocks * 8; e += 128) {
                     const int rr = valid + e / (LY::kLatBlocks * 8);
                     const int rem = e % (LY::kLatBlocks * 8);
-                    *reinterpret_cast<uint4*>(stg + (rem >> 3) * (kTile * 128) + rr * 128 + (rem & 7) * 16) =
+                    *reinterpret_cast<uint4*>(stg + (rem >> 3) * (KT * 128) + rr * 128 + (rem & 7) * 16) =
                         make_uint4(0, 0, 0, 0);
                 }
+            }
+            if (!o_seen && !wait_bounded(odone, (j - 1) & 1, p.status)) {
+                *(volatile int*)abort_flag = 1;
+                late_fail = true;           // acted on, uniformly, at the next tile's vote
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -421,7 +476,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             for (int c16 = 0; c16 < rows_o; c16 += 16) {
                 uint32_t v[16];
                 if (n_t > 0) {
-                    tmem_ld16(tmem + kColO + c * rows_o + c16 + lane_base, v);
+                    tmem_ld16(tmem + LY::kColO + c * rows_o + c16 + lane_base, v);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -620,8 +675,9 @@ combine_var_kernel(const float* __restrict__ o_part, const float* __restrict__ l
 template <int DC, int DR, bool PLAIN, int NST>
 int launch_kernel(const CUtensorMap& lat, const CUtensorMap& rope, const TcParams& tp, int n_rb, int max_items,
                   cudaStream_t s) {
-    using LY = Layout<DC, DR, NST>;
-    auto k = decode_tc_kernel<DC, DR, PLAIN, NST>;
+    constexpr int KT = tile_of<DC>();
+    using LY = Layout<DC, DR, NST, KT>;
+    auto k = decode_tc_kernel<DC, DR, PLAIN, NST, KT>;
     static_assert(LY::kBytes <= 232448, "shared memory budget");
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes) != cudaSuccess)
         return QKMLA_ERR_CUDA;
@@ -671,10 +727,11 @@ bool tc_supported(const qkmla_decode_args* a) {
     if (a->cache_dtype != QKMLA_BF16) return false;
     if (!((a->d_c == 512 && a->d_r == 64) || (a->d_c == 256 && a->d_r == 32))) return false;
     if (a->G > kMaxG || a->B > kMaxB) return false;
-    if (a->page_size % kTile) return false;
+    // a TMA box (64 tokens for d_c = 256, 32 for d_c = 512) never straddles a page
+    if (a->page_size % (a->d_c == 256 ? 64 : 32)) return false;
     const int rows_o = a->H < 64 ? a->H : 64;
     if (rows_o % 16 || a->H % rows_o) return false;
-    if (rows_o > a->d_r) return false;     // P^T (rows_o x 32 tokens) reuses the tile's RoPE slot
+    if (rows_o > a->d_r) return false;     // P^T (rows_o x tile tokens) reuses the tile's RoPE slot
     if (((uintptr_t)a->kv_cache % 16) || ((uintptr_t)a->q_tilde % 16) || ((uintptr_t)a->o % 16)) return false;
     if (!(a->flags & QKMLA_FLAG_PLAIN_MLA) && ((uintptr_t)a->ak_cache % 16)) return false;
     return true;
@@ -715,17 +772,18 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     int* status = device_status_ptr();
     const int max_len = a->max_pages * a->page_size;
 
-    const int tile = pair_shape(a) ? 64 : kTile;
+    const int tile = pair_shape(a) ? 64 : a->d_c == 256 ? tile_of<256>() : tile_of<512>();
+    const int box = tile < 64 ? tile : 64;
     sched_kernel<<<1, 1024, 0, s>>>(a->seq_lens, a->B, a->s_q, max_len, n_rb, sms, /*min_tokens=*/512, tile,
                                     a->num_splits, items, n_items, seq_nsplit, seq_part0, status);
     if (cudaGetLastError() != cudaSuccess) return QKMLA_ERR_CUDA;
 
     CUtensorMap lat, rope;
     const int row = a->d_c + a->d_r;
-    if (!make_map(&lat, a->kv_cache, a->num_slots, row, 64, kTile, CU_TENSOR_MAP_SWIZZLE_128B)) return QKMLA_ERR_CUDA;
+    if (!make_map(&lat, a->kv_cache, a->num_slots, row, 64, box, CU_TENSOR_MAP_SWIZZLE_128B)) return QKMLA_ERR_CUDA;
     if (a->d_r == 64) {
         rope = lat;
-    } else if (!make_map(&rope, a->kv_cache, a->num_slots, row, 32, kTile, CU_TENSOR_MAP_SWIZZLE_64B)) {
+    } else if (!make_map(&rope, a->kv_cache, a->num_slots, row, 32, box, CU_TENSOR_MAP_SWIZZLE_64B)) {
         return QKMLA_ERR_CUDA;
     }
     TcParams tp;
@@ -759,8 +817,8 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
         rc = plain ? launch_kernel<512, 64, true, 4>(lat, rope, tp, n_rb, max_items, s)
                    : launch_kernel<512, 64, false, 4>(lat, rope, tp, n_rb, max_items, s);
     } else {
-        rc = plain ? launch_kernel<256, 32, true, 8>(lat, rope, tp, n_rb, max_items, s)
-                   : launch_kernel<256, 32, false, 8>(lat, rope, tp, n_rb, max_items, s);
+        rc = plain ? launch_kernel<256, 32, true, 2>(lat, rope, tp, n_rb, max_items, s)
+                   : launch_kernel<256, 32, false, 2>(lat, rope, tp, n_rb, max_items, s);
     }
     if (rc != QKMLA_OK) return rc;
     combine_var_kernel<<<a->B * a->s_q * a->H, 128, 0, s>>>(o_part, lse_part, seq_nsplit, seq_part0, a->s_q * a->H,

@@ -197,8 +197,9 @@ CASES = {
     "mixed_sq2_ragged": (4, dict(B=6, lens=(2, 64, 65, 130, 777, 5000))),
     "mixed_sq2_B3": (4, dict(B=3, lens=(512, 4097, 20000))),
     "small_bf16_B3": (1, dict(B=3, lens=(1024, 1500, 8192))),
+    "small_ragged": (1, dict(B=6, lens=(1, 63, 64, 65, 129, 3001))),
 }
-EDGE = {"dsv3_ragged", "mixed_sq2_ragged"}
+EDGE = {"dsv3_ragged", "mixed_sq2_ragged", "small_ragged"}
 
 
 def _workload(name):
