@@ -31,6 +31,8 @@ absorb_kernel(const float* __restrict__ q, const float* __restrict__ gq, const f
     const int M = rows * hpg;
     const int m0 = blockIdx.x * kTM, n0 = blockIdx.y * kTN;
     const int tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
 
     for (int e = tid; e < kTM * d_h; e += kThreads) {
         const int ml = e / d_h, k = e % d_h;
@@ -113,13 +115,16 @@ int launch_absorb(const float* q, const float* gq, const float* gk, const float*
         auto k = absorb_kernel<float>;
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return QKMLA_ERR_CUDA;
-        k<<<grid, kThreads, smem, s>>>(q, gq, gk, wk, rows, H, G, d_h, d_c, eps, plain, (float*)qt, aq);
+        if (launch_pdl(k, grid, dim3(kThreads), smem, s, q, gq, gk, wk, rows, H, G, d_h, d_c, eps, (int)plain,
+                       (float*)qt, aq) != cudaSuccess)
+            return QKMLA_ERR_CUDA;
     } else {
         auto k = absorb_kernel<__nv_bfloat16>;
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return QKMLA_ERR_CUDA;
-        k<<<grid, kThreads, smem, s>>>(q, gq, gk, wk, rows, H, G, d_h, d_c, eps, plain,
-                                       (__nv_bfloat16*)qt, aq);
+        if (launch_pdl(k, grid, dim3(kThreads), smem, s, q, gq, gk, wk, rows, H, G, d_h, d_c, eps, (int)plain,
+                       (__nv_bfloat16*)qt, aq) != cudaSuccess)
+            return QKMLA_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
 }

@@ -98,6 +98,8 @@ absorb_tc_kernel(const float* __restrict__ q, const float* __restrict__ gq, cons
         tmem_relinquish();
     }
     __syncthreads();
+    pdl_wait();
+    pdl_trigger();
     // ---- every operand byte in flight at once ----
     if (tid == 0) mbar_arrive_expect_tx(&bar[0], (uint32_t)(m_valid * DH * 4 + LY::kB));
     if (tid < m_valid) {
@@ -264,9 +266,10 @@ int launch_t(const float* q, const float* gq, const float* gk, const float* wk, 
         return QKMLA_ERR_CUDA;
     const int M = rows * (H / G);
     dim3 grid((M + kM - 1) / kM, d_c / kN, G);
-    k<<<grid, kThreads, LY::kBytes, s>>>(q, gq, gk, wk, rows, H, G, d_c, eps, plain ? 1 : 0, (OutT*)qt, aq,
-                                         device_status_ptr());
-    return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
+    return launch_pdl(k, grid, dim3(kThreads), LY::kBytes, s, q, gq, gk, wk, rows, H, G, d_c, eps, plain ? 1 : 0,
+                      (OutT*)qt, aq, device_status_ptr()) == cudaSuccess
+               ? QKMLA_OK
+               : QKMLA_ERR_CUDA;
 }
 
 }  // namespace

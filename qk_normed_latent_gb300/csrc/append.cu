@@ -98,6 +98,8 @@ append_bulk_kernel(const float* __restrict__ c_new, const float* __restrict__ r_
         fence_barrier_init();
     }
     __syncthreads();
+    pdl_wait();
+    pdl_trigger();
     if (tid == 0) {
         mbar_arrive_expect_tx(&bars[0], (uint32_t)(nvalid * d_c * 4));
         for (int t = 0; t < nvalid; ++t)
@@ -211,6 +213,8 @@ append_plain_kernel(const float* __restrict__ c_new, const float* __restrict__ r
     const int n0 = blockIdx.x * kTT;
     const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;   // ty: 0..7
     const int nj = (d_h + 31) / 32;
+    pdl_wait();
+    pdl_trigger();
 
     float acc[4][kMaxJ];
 #pragma unroll
@@ -290,16 +294,18 @@ int launch_t(const float* c_new, const float* r_new, const float* wk, const floa
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bulk) != cudaSuccess)
             return QKMLA_ERR_CUDA;
         dim3 grid((N + ft - 1) / ft, G);
-        k<<<grid, kThreads, smem_bulk, s>>>(c_new, r_new, wk, grk, slots, N, G, d_c, d_h, d_r, eps, plain, kv, ak,
-                                            num_slots, device_status_ptr());
+        if (launch_pdl(k, grid, dim3(kThreads), smem_bulk, s, c_new, r_new, wk, grk, slots, N, G, d_c, d_h, d_r, eps,
+                       (int)plain, kv, ak, num_slots, device_status_ptr()) != cudaSuccess)
+            return QKMLA_ERR_CUDA;
     } else {
         auto k = append_plain_kernel<CT>;
         const size_t smem = (size_t)kKC * d_h * sizeof(float);
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return QKMLA_ERR_CUDA;
         dim3 grid((N + kTT - 1) / kTT, G);
-        k<<<grid, kThreads, smem, s>>>(c_new, r_new, wk, grk, slots, N, G, d_c, d_h, d_r, eps, plain, kv, ak,
-                                       num_slots, device_status_ptr());
+        if (launch_pdl(k, grid, dim3(kThreads), smem, s, c_new, r_new, wk, grk, slots, N, G, d_c, d_h, d_r, eps,
+                       (int)plain, kv, ak, num_slots, device_status_ptr()) != cudaSuccess)
+            return QKMLA_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
 }

@@ -22,6 +22,8 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_p
     const int64_t rh = blockIdx.x;
     const int tid = threadIdx.x;
     const float* lp = lse_part + rh * nsplit;
+    pdl_wait();
+    pdl_trigger();
 
     float m = -INFINITY;
     for (int s = tid; s < nsplit; s += kThreads) m = fmaxf(m, lp[s]);
@@ -73,8 +75,10 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_p
 int launch_combine(const float* o_part, const float* lse_part, int rows, int nsplit, int d_c, void* o,
                    int o_dtype, float* lse, cudaStream_t s) {
     if (nsplit > kMaxSplits) return QKMLA_ERR_UNSUPPORTED;
-    combine_kernel<<<rows, kThreads, 0, s>>>(o_part, lse_part, nsplit, d_c, o, o_dtype, lse);
-    return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
+    return launch_pdl(combine_kernel, dim3(rows), dim3(kThreads), 0, s, o_part, lse_part, nsplit, d_c, o, o_dtype,
+                      lse) == cudaSuccess
+               ? QKMLA_OK
+               : QKMLA_ERR_CUDA;
 }
 
 }  // namespace qkmla

@@ -15,6 +15,15 @@ __device__ __forceinline__ void report(int* st, int code) {
     if (st) atomicCAS(st, 0, code);
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialization: it may start while the previous kernel on
+// the stream is still running, so it first does only work that touches no
+// global memory, then waits (pdl_wait) until the previous grid has completed and
+// its writes are visible, and then lets the next kernel start its own launch
+// (pdl_trigger).  Launched without the attribute, both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 template <typename T> struct Elem;
 template <> struct Elem<float> {
     static __device__ __forceinline__ float load(const float* p) { return *p; }
@@ -54,6 +63,23 @@ __device__ __forceinline__ int64_t slot_of(const int32_t* page_table, int b, int
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+
+// Host: launch `kernel` on `s` with programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace qkmla
 

@@ -100,6 +100,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     float* coef_s = (float*)(sm + kOffMisc + kNumBars * 8 + 16);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();
+    pdl_trigger();
     if ((int)blockIdx.y >= *p.n_items) return;          // uniform over the cluster
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
@@ -496,8 +498,8 @@ int launch_pair(const qkmla_decode_args* a, const TcParams& tp, int max_items, c
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytesP) != cudaSuccess)
         return QKMLA_ERR_CUDA;
     dim3 grid(2 * a->s_q, max_items);
-    k<<<grid, kThreadsP, kBytesP, s>>>(lat, rope, tp);
-    return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
+    return launch_pdl(k, grid, dim3(kThreadsP), kBytesP, s, lat, rope, tp) == cudaSuccess ? QKMLA_OK
+                                                                                       : QKMLA_ERR_CUDA;
 }
 
 }  // namespace dec

@@ -71,6 +71,8 @@ decode_simt_kernel(SimtParams p) {
     const CT* kv = (const CT*)p.kv;
     const float l2e = kLog2e;
 
+    pdl_wait();
+    pdl_trigger();
     const int seq_len = p.seq_lens[b];
     const bool bad_len = seq_len < p.s_q || seq_len > p.max_pages * p.page_size;
     if (bad_len && tid == 0) report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
@@ -220,8 +222,7 @@ int launch_t(const SimtParams& p, cudaStream_t s) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return QKMLA_ERR_CUDA;
     dim3 grid(p.B * p.s_q * p.G, p.nsplit);
-    k<<<grid, kThreads, smem, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
+    return launch_pdl(k, grid, dim3(kThreads), smem, s, p) == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
 }
 
 template <typename CT, int NJ>

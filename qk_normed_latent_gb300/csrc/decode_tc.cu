@@ -42,20 +42,18 @@ using namespace dec;
 constexpr int kRowsMMA = 64;       // M of the logit MMA
 constexpr int kThreads = 192;
 
-// Tokens per tile: 128 for d_c = 256 (the logit MMA count per tile does not grow
-// with N up to 128, so wide tiles cut the MMA cost per token fourfold), 32 for
-// d_c = 512 (its Q tile and stages leave no room for wider ones).  A tile is
-// loaded in boxes of at most 64 tokens, each mapped through the page table.
+// Tokens per tile: 64 for d_c = 256, 32 for d_c = 512.  The logit MMA costs the
+// same issue time for any N up to 128, so wider tiles cut its cost per token; the
+// width is bounded by the TMA ring, which needs about three stages in flight to
+// cover DRAM latency (stage = one tile, one TMA box, one page-table lookup).
 template <int DC>
-constexpr int tile_of() { return DC == 256 ? 128 : 32; }
+constexpr int tile_of() { return DC == 256 ? 64 : 32; }
 
 // ---------------------------------------------------------------------------
 // shared-memory layout
 // ---------------------------------------------------------------------------
 template <int DC, int DR, int NST, int KT>
 struct Layout {
-    static constexpr int kBox = KT < 64 ? KT : 64;                  // tokens per TMA box
-    static constexpr int kSub = KT / kBox;                          // boxes per tile
     static constexpr int kLatBlocks = DC / 64;                      // 64-column TMA boxes
     static constexpr int kRopeRowBytes = DR * 2;                    // 128 (SW128) or 64 (SW64)
     static constexpr int kQLat = kLatBlocks * kRowsMMA * 128;
@@ -73,13 +71,13 @@ struct Layout {
     static constexpr int kNSB = (4 * KT + kChunks * 64 <= 512) ? 2 : 1;
     static constexpr uint32_t kColSc = 0, kColSr = kNSB * KT, kColO = 2 * kNSB * KT;
     // misc: barriers then per-row arrays
-    static constexpr int kNumBars = 3 * NST + 2 * kNSB + 1;
+    static constexpr int kNumBars = 3 * NST + 2 * kNSB + 2;
     static constexpr int kMisc = kNumBars * 8 + 16 + 4 * kRowsMMA * 4;
     static constexpr int kBytes = kOffMisc + kMisc + 1024;        // + alignment slack
-    // bytes one box brings: latent blocks + RoPE rows (alpha^k is added at run time)
-    static constexpr uint32_t kBoxTx = (uint32_t)(kLatBlocks * kBox * 128 + kBox * kRopeRowBytes);
+    // bytes one tile brings: latent blocks + RoPE rows (alpha^k is added at run time)
+    static constexpr uint32_t kTileTx = (uint32_t)(kLatBlocks * KT * 128 + KT * kRopeRowBytes);
     static_assert(kColO + kChunks * 64 <= 512, "TMEM budget");
-    static_assert(KT % 32 == 0 && KT <= 128, "tile");
+    static_assert(KT == 32 || KT == 64, "a tile is one TMA box of a 32- or 64-token page piece");
 };
 
 constexpr uint32_t kTmemCols = 512;
@@ -96,7 +94,7 @@ __device__ __forceinline__ uint32_t pt_offset(int r, int t, int rows_o) {
 template <int DC, int DR, bool PLAIN, int NST, int KT>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
-                 const TcParams p) {
+                 const __grid_constant__ CUtensorMap tm_q, const TcParams p) {
     using LY = Layout<DC, DR, NST, KT>;
     constexpr int kChunks = LY::kChunks;
     constexpr int NSB = LY::kNSB;
@@ -110,6 +108,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
     uint64_t* sfull = bars + 3 * NST;        // [NSB] logit MMA done -> softmax
     uint64_t* sfree = sfull + NSB;           // [NSB] softmax read S -> MMA
     uint64_t* odone = sfree + NSB;           // output MMA of a tile done
+    uint64_t* qfull = odone + 1;             // Q~ tile landed
     uint32_t* tmem_slot = (uint32_t*)(bars + LY::kNumBars);
     int* abort_flag = (int*)(tmem_slot + 1);
     float* coef_s = (float*)(sm + LY::kOffMisc + LY::kNumBars * 8 + 16);
@@ -118,6 +117,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int item_idx = blockIdx.y;
+    pdl_wait();
+    pdl_trigger();
     if (item_idx >= *p.n_items) return;
     const WorkItem it = p.items[item_idx];
     const int rows_o = p.rows_o;
@@ -145,21 +146,63 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
         fence_barrier_init();
         prefetch_tmap(&tm_lat);
         if (DR != 64) prefetch_tmap(&tm_rope);
+        prefetch_tmap(&tm_q);
     }
+    __syncthreads();
+    const size_t qrow0 = ((size_t)b * p.s_q + qi) * p.H + h0;
+
+    // ---- TMA producer state (warp 0): the slot of tile j + lane, 32 tiles at a time ----
+    auto slot_of_tile = [&](int j) -> int64_t {
+        if (j >= n_t) return 0;
+        const int t0 = (jt0 + j) * KT;
+        const int pg = t0 / p.page_size;
+        int64_t page = p.page_table ? (int64_t)p.page_table[(int64_t)b * p.max_pages + pg]
+                                    : (int64_t)b * p.max_pages + pg;
+        if (page < 0 || page >= p.num_pages) {
+            report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
+            page = 0;
+        }
+        return page * p.page_size + (t0 % p.page_size);
+    };
+    const uint32_t ak_bytes = PLAIN ? 0u : (uint32_t)(KT * p.G * 4);
+    auto issue_tile = [&](int j, int64_t slot0) {        // lane 0 of warp 0
+        const int s = j % NST;
+        uint8_t* stg = sm + LY::kOffStage + s * LY::kStage;
+        mbar_arrive_expect_tx(&full[s], LY::kTileTx + ak_bytes);
+#pragma unroll
+        for (int blk = 0; blk < LY::kLatBlocks; ++blk)
+            tma_load_2d(stg + blk * (KT * 128), &tm_lat, blk * 64, (int)slot0, &full[s]);
+        if (DR == 64)
+            tma_load_2d(stg + LY::kSLat, &tm_lat, DC, (int)slot0, &full[s]);
+        else
+            tma_load_2d(stg + LY::kSLat, &tm_rope, DC, (int)slot0, &full[s]);
+        if (!PLAIN) bulk_load(stg + LY::kSLat + LY::kSRope, p.ak + slot0 * p.G, ak_bytes, &full[s]);
+    };
+    int64_t slot_batch = 0;
+
     if (warp == 0) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
-    }
-
-    // ---- prologue (softmax warps): stage Q~ and the normalised RoPE query ----
-    if (warp >= 2) {
+        // the Q~ tile and the first NST tiles go out before the prologue barrier
+        slot_batch = slot_of_tile(lane);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(qfull, (uint32_t)(LY::kLatBlocks * rows_o * 128));
+#pragma unroll
+            for (int blk = 0; blk < LY::kLatBlocks; ++blk)
+                tma_load_2d(sQ + blk * (kRowsMMA * 128), &tm_q, blk * 64, (int)qrow0, qfull);
+        }
+        for (int j = 0; j < NST && j < n_t; ++j) {
+            const int64_t slot0 = __shfl_sync(0xffffffffu, slot_batch, j);
+            if (lane == 0) issue_tile(j, slot0);
+        }
+    } else if (warp >= 2) {
+        // ---- prologue (softmax warps): the normalised RoPE query, alpha^q, and
+        //      zero Q~ rows past rows_o (the TMA fills rows 0 .. rows_o-1) ----
         const int st = tid - 64;
-        const size_t qrow0 = ((size_t)b * p.s_q + qi) * p.H + h0;
-        for (int e = st; e < kRowsMMA * (DC / 8); e += 128) {
-            const int r = e / (DC / 8), k = e % (DC / 8);
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < rows_o) v = *reinterpret_cast<const uint4*>(p.qt + (qrow0 + r) * DC + k * 8);
-            *reinterpret_cast<uint4*>(sQ + (k >> 3) * (kRowsMMA * 128) + sw128_offset(r, (k & 7) * 8)) = v;
+        for (int e = st; e < (kRowsMMA - rows_o) * 8 * LY::kLatBlocks; e += 128) {
+            const int r = rows_o + e / (8 * LY::kLatBlocks), rem = e % (8 * LY::kLatBlocks);
+            *reinterpret_cast<uint4*>(sQ + (rem >> 3) * (kRowsMMA * 128) + r * 128 + (rem & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
         }
         // RoPE query: two threads per row
         {
@@ -199,45 +242,23 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ===================== TMA producer =====================
-        if (lane == 0) {
-            for (int j = 0; j < n_t; ++j) {
+        // ===================== TMA producer (lane 0 issues; lanes hold page slots) =====================
+        for (int j = NST; j < n_t; ++j) {
+            if ((j & 31) == 0) slot_batch = slot_of_tile(j + lane);
+            const int64_t slot0 = __shfl_sync(0xffffffffu, slot_batch, j & 31);
+            int go = 1;
+            if (lane == 0) {
                 const int s = j % NST;
-                if (j >= NST && !wait_bounded(&empty[s], ((j / NST) - 1) & 1, p.status)) {
+                if (!wait_bounded(&empty[s], ((j / NST) - 1) & 1, p.status)) {
                     *abort_flag = 1;
-                    break;
-                }
-                if (*(volatile int*)abort_flag) break;
-                const int t0 = (jt0 + j) * KT;
-                // boxes wholly past the end of the sequence are not loaded
-                const int n_sub = min(LY::kSub, (L - t0 + LY::kBox - 1) / LY::kBox);
-                uint8_t* stg = sm + LY::kOffStage + s * LY::kStage;
-                const uint32_t ak_bytes = PLAIN ? 0u : (uint32_t)(LY::kBox * p.G * 4);
-                mbar_arrive_expect_tx(&full[s], (uint32_t)n_sub * (LY::kBoxTx + ak_bytes));
-                for (int h = 0; h < n_sub; ++h) {
-                    const int tb = t0 + h * LY::kBox;
-                    const int pg = tb / p.page_size;
-                    int64_t page = p.page_table ? (int64_t)p.page_table[(int64_t)b * p.max_pages + pg]
-                                                : (int64_t)b * p.max_pages + pg;
-                    if (page < 0 || page >= p.num_pages) {
-                        report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
-                        page = 0;
-                    }
-                    const int64_t slot0 = page * p.page_size + (tb % p.page_size);
-#pragma unroll
-                    for (int blk = 0; blk < LY::kLatBlocks; ++blk)
-                        tma_load_2d(stg + blk * (KT * 128) + h * (LY::kBox * 128), &tm_lat, blk * 64, (int)slot0,
-                                    &full[s]);
-                    uint8_t* rope_dst = stg + LY::kSLat + h * (LY::kBox * LY::kRopeRowBytes);
-                    if (DR == 64)
-                        tma_load_2d(rope_dst, &tm_lat, DC, (int)slot0, &full[s]);
-                    else
-                        tma_load_2d(rope_dst, &tm_rope, DC, (int)slot0, &full[s]);
-                    if (!PLAIN)
-                        bulk_load(stg + LY::kSLat + LY::kSRope + h * (LY::kBox * p.G * 4), p.ak + slot0 * p.G,
-                                  ak_bytes, &full[s]);
+                    go = 0;
+                } else if (*(volatile int*)abort_flag) {
+                    go = 0;
+                } else {
+                    issue_tile(j, slot0);
                 }
             }
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
@@ -270,7 +291,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                 mma_commit(odone);
                 return true;
             };
-            bool ok = true;
+            // always waited, so no CTA exits with the Q~ copy in flight
+            bool ok = wait_bounded(qfull, 0, p.status);
             for (int j = 0; j < n_t && ok; ++j) {
                 const int s = j % NST, sb = j % NSB;
                 if (!wait_bounded(&full[s], (j / NST) & 1, p.status)) { ok = false; break; }
@@ -521,6 +543,8 @@ sched_kernel(const int32_t* __restrict__ seq_lens, int B, int s_q, int max_len, 
     __shared__ int red[32];
     __shared__ int s_total, s_tpi;
     const int tid = threadIdx.x, nt = blockDim.x;
+    pdl_wait();
+    pdl_trigger();
     int tot = 0, mx = 0;
     for (int b = tid; b < B; b += nt) {
         const int L = seq_lens[b];
@@ -611,6 +635,8 @@ combine_var_kernel(const float* __restrict__ o_part, const float* __restrict__ l
     __shared__ float s_inv, s_lse;
     const int row = blockIdx.x;                 // (b, i, h)
     const int b = row / rows_per_seq, rr = row % rows_per_seq;
+    pdl_wait();
+    pdl_trigger();
     const int ns = seq_nsplit[b];
     if (ns <= 1) return;
     const int p0 = seq_part0[b];
@@ -673,8 +699,8 @@ combine_var_kernel(const float* __restrict__ o_part, const float* __restrict__ l
 // host side
 // ---------------------------------------------------------------------------
 template <int DC, int DR, bool PLAIN, int NST>
-int launch_kernel(const CUtensorMap& lat, const CUtensorMap& rope, const TcParams& tp, int n_rb, int max_items,
-                  cudaStream_t s) {
+int launch_kernel(const CUtensorMap& lat, const CUtensorMap& rope, const CUtensorMap& qmap, const TcParams& tp,
+                  int n_rb, int max_items, cudaStream_t s) {
     constexpr int KT = tile_of<DC>();
     using LY = Layout<DC, DR, NST, KT>;
     auto k = decode_tc_kernel<DC, DR, PLAIN, NST, KT>;
@@ -682,8 +708,8 @@ int launch_kernel(const CUtensorMap& lat, const CUtensorMap& rope, const TcParam
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes) != cudaSuccess)
         return QKMLA_ERR_CUDA;
     dim3 grid(n_rb, max_items);
-    k<<<grid, kThreads, LY::kBytes, s>>>(lat, rope, tp);
-    return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
+    return launch_pdl(k, grid, dim3(kThreads), LY::kBytes, s, lat, rope, qmap, tp) == cudaSuccess ? QKMLA_OK
+                                                                                         : QKMLA_ERR_CUDA;
 }
 
 }  // namespace
@@ -727,7 +753,7 @@ bool tc_supported(const qkmla_decode_args* a) {
     if (a->cache_dtype != QKMLA_BF16) return false;
     if (!((a->d_c == 512 && a->d_r == 64) || (a->d_c == 256 && a->d_r == 32))) return false;
     if (a->G > kMaxG || a->B > kMaxB) return false;
-    // a TMA box (64 tokens for d_c = 256, 32 for d_c = 512) never straddles a page
+    // a tile (64 tokens for d_c = 256, 32 for d_c = 512) never straddles a page
     if (a->page_size % (a->d_c == 256 ? 64 : 32)) return false;
     const int rows_o = a->H < 64 ? a->H : 64;
     if (rows_o % 16 || a->H % rows_o) return false;
@@ -773,10 +799,11 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     const int max_len = a->max_pages * a->page_size;
 
     const int tile = pair_shape(a) ? 64 : a->d_c == 256 ? tile_of<256>() : tile_of<512>();
-    const int box = tile < 64 ? tile : 64;
-    sched_kernel<<<1, 1024, 0, s>>>(a->seq_lens, a->B, a->s_q, max_len, n_rb, sms, /*min_tokens=*/512, tile,
-                                    a->num_splits, items, n_items, seq_nsplit, seq_part0, status);
-    if (cudaGetLastError() != cudaSuccess) return QKMLA_ERR_CUDA;
+    const int box = tile;
+    if (launch_pdl(sched_kernel, dim3(1), dim3(1024), 0, s, a->seq_lens, a->B, a->s_q, max_len, n_rb, sms,
+                   /*min_tokens=*/512, tile, a->num_splits, items, n_items, seq_nsplit, seq_part0, status) !=
+        cudaSuccess)
+        return QKMLA_ERR_CUDA;
 
     CUtensorMap lat, rope;
     const int row = a->d_c + a->d_r;
@@ -786,6 +813,10 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     } else if (!make_map(&rope, a->kv_cache, a->num_slots, row, 32, box, CU_TENSOR_MAP_SWIZZLE_64B)) {
         return QKMLA_ERR_CUDA;
     }
+    CUtensorMap qmap;
+    if (!pair_shape(a) && !make_map(&qmap, a->q_tilde, (int64_t)a->B * a->s_q * a->H, a->d_c, 64, rows_o,
+                                    CU_TENSOR_MAP_SWIZZLE_128B))
+        return QKMLA_ERR_CUDA;
     TcParams tp;
     tp.qt = (const __nv_bfloat16*)a->q_tilde;
     tp.aq = a->alpha_q;
@@ -814,16 +845,18 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     if (pair_shape(a)) {
         rc = launch_pair(a, tp, max_items, s);
     } else if (a->d_c == 512) {
-        rc = plain ? launch_kernel<512, 64, true, 4>(lat, rope, tp, n_rb, max_items, s)
-                   : launch_kernel<512, 64, false, 4>(lat, rope, tp, n_rb, max_items, s);
+        rc = plain ? launch_kernel<512, 64, true, 4>(lat, rope, qmap, tp, n_rb, max_items, s)
+                   : launch_kernel<512, 64, false, 4>(lat, rope, qmap, tp, n_rb, max_items, s);
     } else {
-        rc = plain ? launch_kernel<256, 32, true, 2>(lat, rope, tp, n_rb, max_items, s)
-                   : launch_kernel<256, 32, false, 2>(lat, rope, tp, n_rb, max_items, s);
+        rc = plain ? launch_kernel<256, 32, true, 4>(lat, rope, qmap, tp, n_rb, max_items, s)
+                   : launch_kernel<256, 32, false, 4>(lat, rope, qmap, tp, n_rb, max_items, s);
     }
     if (rc != QKMLA_OK) return rc;
-    combine_var_kernel<<<a->B * a->s_q * a->H, 128, 0, s>>>(o_part, lse_part, seq_nsplit, seq_part0, a->s_q * a->H,
-                                                             a->d_c, a->o, a->o_dtype, a->lse);
-    return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
+    return launch_pdl(combine_var_kernel, dim3(a->B * a->s_q * a->H), dim3(128), 0, s, (const float*)o_part,
+                      (const float*)lse_part, (const int*)seq_nsplit, (const int*)seq_part0, a->s_q * a->H, a->d_c,
+                      a->o, a->o_dtype, a->lse) == cudaSuccess
+               ? QKMLA_OK
+               : QKMLA_ERR_CUDA;
 }
 
 }  // namespace qkmla
