@@ -17,18 +17,25 @@
 //     and applies the alpha^q / alpha^k scaling to its content part (the
 //     scaling is linear, so partial logits add),
 //   * exchanges partials with the other CTA: every softmax warp stages its 32
-//     rows locally and sends them with one bulk copy into the other CTA's
-//     shared memory (completing on a per-warp mbarrier there), then adds the
-//     rows it received -- fp32 addition commutes, so both CTAs hold
-//     bit-identical logits and P,
+//     rows -- 64 fp16 values relative to the row's own maximum, plus that
+//     maximum in fp32, so the values near the maximum (the ones that matter
+//     after exp) keep ~11 bits -- and sends them with one bulk copy into the
+//     other CTA's shared memory (completing on a per-warp mbarrier there); each
+//     CTA adds the received rows to its own fp32 partials,
 //   * writes P (bf16) into TMEM and accumulates O = P C over its 256 latents
 //     (M=128 rows, N=256, K=64 tokens, A read from TMEM).
-// Each CTA streams only its half of every tile from HBM.
+// Each CTA streams only its half of every tile from HBM, through three stages:
+// a stage stays busy until its tile's output MMA, so the third one keeps a load
+// in flight while the other two are being used.
 //
 // Warps: 0 TMA producer (+ TMEM owner), 1 MMA issuer, 2-5 softmax / exchange /
-// epilogue (thread = query row = TMEM lane).  Softmax warps run independently
-// (each owns 32 rows end to end).  All waits are bounded (2 s).
+// epilogue (thread = query row = TMEM lane).  The MMA issuer polls its two
+// inputs (a landed tile, a written P) and issues whichever is ready, so an
+// output MMA -- and the stage it frees -- never waits behind the next tile's
+// load.  All waits are bounded (2 s).
 #include <cudaTypedefs.h>
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "decode_common.cuh"
@@ -44,6 +51,7 @@ constexpr int kDC = 512, kDR = 64;
 constexpr int kHalfLat = kDC / 2;  // latent columns per CTA
 constexpr int kHalfRope = kDR / 2; // RoPE columns per CTA
 constexpr int kThreadsP = 192;
+constexpr int kNst = 3;            // TMA stages
 
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr int kQLat = 4 * kR * 128;                    // Q~ half: 4 blocks of 128 rows x 128 B
@@ -52,29 +60,25 @@ constexpr int kSLat = 4 * kT * 128;                    // tile half: 4 boxes of 
 constexpr int kSRope = kT * 64;                        // 64 tokens x 64 B
 constexpr int kSAk = kT * kMaxG * 4;
 constexpr int kStageB = kSLat + kSRope + kSAk;         // 38 KB
-constexpr int kXB = kR * kT * 4;                       // 128 rows x 64 fp32 (8 KB per softmax warp)
+// exchange row: 64 fp16 partial logits minus the row maximum (128 B), the
+// maximum (fp32), padding to 144 B (conflict-free 16-byte accesses by 32 rows)
+constexpr int kXRow = 144;
+constexpr int kXSlice = 32 * kXRow;                    // one softmax warp's 32 rows
+constexpr int kXB = 4 * kXSlice;
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kQLat + kQRope;
-constexpr int kOffX = kOffStage + 2 * kStageB;         // received partials
-constexpr int kOffY = kOffX + kXB;                     // own partials (sent), then P
+constexpr int kOffX = kOffStage + kNst * kStageB;      // received partials
+constexpr int kOffY = kOffX + kXB;                     // own partials (sent)
 constexpr int kOffMisc = kOffY + kXB;
-constexpr int kNumBars = 19;
+constexpr int kNumBars = 20;
 constexpr int kBytesP = kOffMisc + kNumBars * 8 + 16 + kR * 4 + 1024;
-static_assert(kStageB % 1024 == 0 && kOffStage % 1024 == 0 && kOffX % 1024 == 0 && kOffY % 1024 == 0, "align");
+static_assert(kStageB % 1024 == 0 && kOffStage % 1024 == 0 && kOffX % 16 == 0 && kOffY % 16 == 0, "align");
+static_assert(kXSlice % 16 == 0, "bulk copy size");
 static_assert(kBytesP <= 232448, "shared memory budget");
 
 // TMEM columns: S_c at 0, S_r at 64, P[2] (64 bf16 tokens = 32 columns each) at
 // 128 / 160, O (128 rows x 256 latents) at 256
 constexpr uint32_t kCSc = 0, kCSr = 64, kCP = 128, kCO = 256;
-
-// Byte offset of floats 4k..4k+3 of row r in an exchange buffer: rows of 256 B,
-// 16-byte chunks XOR-swizzled; rows 32w..32w+31 form warp w's 8 KB slice.
-__device__ __forceinline__ uint32_t xoff(int r, int k) { return (uint32_t)(r * 256 + (((k ^ r) & 15) << 4)); }
-// P (A operand of the output MMA): K-major, 128-byte swizzle, 8-row groups
-// 2048 B apart so that warp w's 32 rows stay inside its own 8 KB slice.
-__device__ __forceinline__ uint32_t poff(int r, int col) {
-    return (uint32_t)((r >> 3) * 2048 + (r & 7) * 128 + ((((col >> 3) ^ (r & 7)) & 7) << 4) + (col & 7) * 2);
-}
 
 template <bool PLAIN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsP, 1)
@@ -86,15 +90,14 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     uint8_t* sX = sm + kOffX;
     uint8_t* sY = sm + kOffY;
     uint64_t* bars = (uint64_t*)(sm + kOffMisc);
-    uint64_t* full = bars;          // [2] TMA -> MMA
-    uint64_t* empty = bars + 2;     // [2] output MMA done -> TMA
-    uint64_t* sfull = bars + 4;     // logit MMA done -> softmax (one S buffer)
-    uint64_t* sfree = bars + 5;     // softmax read S -> MMA
-    uint64_t* pdone = bars + 6;     // [2] output MMA done with P buffer -> softmax
-    uint64_t* pfull = bars + 8;     // [2] P written -> output MMA
-    // bars + 10: spare
-    uint64_t* xfull = bars + 11;    // [4] per warp: the other CTA's partial rows landed in X
-    uint64_t* xfree = bars + 15;    // [4] per warp: the other CTA's X rows may be overwritten
+    uint64_t* full = bars;          // [3] TMA -> MMA
+    uint64_t* empty = bars + 3;     // [3] output MMA done -> TMA
+    uint64_t* sfull = bars + 6;     // logit MMA done -> softmax (one S buffer)
+    uint64_t* sfree = bars + 7;     // softmax read S -> MMA
+    uint64_t* pdone = bars + 8;     // [2] output MMA done with P buffer -> softmax
+    uint64_t* pfull = bars + 10;    // [2] P written -> output MMA
+    uint64_t* xfull = bars + 12;    // [4] per warp: the other CTA's partial rows landed in X
+    uint64_t* xfree = bars + 16;    // [4] per warp: the other CTA's X rows may be overwritten
     uint32_t* tmem_slot = (uint32_t*)(bars + kNumBars);
     int* abort_flag = (int*)(tmem_slot + 1);
     float* coef_s = (float*)(sm + kOffMisc + kNumBars * 8 + 16);
@@ -119,7 +122,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     if (tid == 0) {
         if (bad && rank == 0) report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
         for (int i = 0; i < kNumBars; ++i) {
-            const bool four = (i == 5 || i == 8 || i == 9);   // sfree, pfull: one per softmax warp
+            const bool four = (i == 7 || i == 10 || i == 11);   // sfree, pfull: one per softmax warp
             mbar_init(&bars[i], four ? 4u : 1u);
         }
         *abort_flag = 0;
@@ -161,7 +164,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             coef_s[r] = PLAIN ? 0.f : p.scale * p.aq[qrow0 + r] * kLog2e;
         }
         fence_proxy_async_smem();
-        if (lane == 0 && n_t > 0) mbar_arrive_expect_tx(&xfull[warp & 3], kXB / 4);   // tile 0's rows
+        if (lane == 0 && n_t > 0) mbar_arrive_expect_tx(&xfull[warp & 3], kXSlice);   // tile 0's rows
     }
     tc_fence_before();
     cluster_sync();            // both CTAs' barriers exist before any remote access
@@ -170,71 +173,54 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
 
     if (warp == 0) {
         // ===================== TMA producer: this CTA's half of each tile =====================
-        if (lane == 0) {
-            const uint32_t tx = (uint32_t)(kSLat + kSRope) + (PLAIN ? 0u : (uint32_t)(kT * p.G * 4));
-            auto slot_of_tile = [&](int j) -> int {
-                const int t0 = (jt0 + j) * kT;
-                const int pg = t0 / p.page_size;
-                int64_t page = p.page_table ? (int64_t)p.page_table[(int64_t)b * p.max_pages + pg]
-                                            : (int64_t)b * p.max_pages + pg;
-                if (page < 0 || page >= p.num_pages) {
-                    report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
-                    page = 0;
-                }
-                return (int)(page * p.page_size + (t0 % p.page_size));
-            };
-            for (int j = 0; j < n_t && j < 2; ++j) {       // L2 prefetch of the first tiles
-                const int sl = slot_of_tile(j);
-                for (int blk = 0; blk < 4; ++blk) tma_prefetch_l2(&tm_lat, rank * kHalfLat + blk * 64, sl);
+        // lane l holds the slot of tile (j & ~31) + l: 32 page-table reads in parallel
+        auto slot_of_tile = [&](int j) -> int {
+            if (j >= n_t) return 0;
+            const int t0 = (jt0 + j) * kT;
+            const int pg = t0 / p.page_size;
+            int64_t page = p.page_table ? (int64_t)p.page_table[(int64_t)b * p.max_pages + pg]
+                                        : (int64_t)b * p.max_pages + pg;
+            if (page < 0 || page >= p.num_pages) {
+                report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
+                page = 0;
             }
-            for (int j = 0; j < n_t; ++j) {
-                const int s = j & 1;
-                if (j + 2 < n_t) {                          // two tiles ahead into L2
-                    const int sl = slot_of_tile(j + 2);
-                    for (int blk = 0; blk < 4; ++blk) tma_prefetch_l2(&tm_lat, rank * kHalfLat + blk * 64, sl);
-                    tma_prefetch_l2(&tm_rope, kDC + rank * kHalfRope, sl);
-                }
-                if (j >= 2 && !wait_bounded(&empty[s], ((j >> 1) - 1) & 1, p.status)) { *abort_flag = 1; break; }
-                if (*(volatile int*)abort_flag) break;
-                const int slot0 = slot_of_tile(j);
-                uint8_t* stg = sm + kOffStage + s * kStageB;
-                mbar_arrive_expect_tx(&full[s], tx);
+            return (int)(page * p.page_size + (t0 % p.page_size));
+        };
+        const uint32_t tx = (uint32_t)(kSLat + kSRope) + (PLAIN ? 0u : (uint32_t)(kT * p.G * 4));
+        int slot_batch = slot_of_tile(lane);
+        for (int j = 0; j < n_t; ++j) {
+            if ((j & 31) == 0 && j > 0) slot_batch = slot_of_tile(j + lane);
+            const int slot0 = __shfl_sync(0xffffffffu, slot_batch, j & 31);
+            int go = 1;
+            if (lane == 0) {
+                const int s = j % kNst;
+                if (j >= kNst && !wait_bounded(&empty[s], ((j / kNst) - 1) & 1, p.status)) {
+                    *abort_flag = 1;
+                    go = 0;
+                } else if (*(volatile int*)abort_flag) {
+                    go = 0;
+                } else {
+                    uint8_t* stg = sm + kOffStage + s * kStageB;
+                    mbar_arrive_expect_tx(&full[s], tx);
 #pragma unroll
-                for (int blk = 0; blk < 4; ++blk)
-                    tma_load_2d(stg + blk * (kT * 128), &tm_lat, rank * kHalfLat + blk * 64, slot0, &full[s]);
-                tma_load_2d(stg + kSLat, &tm_rope, kDC + rank * kHalfRope, slot0, &full[s]);
-                if (!PLAIN) bulk_load(stg + kSLat + kSRope, p.ak + (int64_t)slot0 * p.G, (uint32_t)(kT * p.G * 4), &full[s]);
+                    for (int blk = 0; blk < 4; ++blk)
+                        tma_load_2d(stg + blk * (kT * 128), &tm_lat, rank * kHalfLat + blk * 64, slot0, &full[s]);
+                    tma_load_2d(stg + kSLat, &tm_rope, kDC + rank * kHalfRope, slot0, &full[s]);
+                    if (!PLAIN)
+                        bulk_load(stg + kSLat + kSRope, p.ak + (int64_t)slot0 * p.G, (uint32_t)(kT * p.G * 4),
+                                  &full[s]);
+                }
             }
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
         }
     } else if (warp == 1) {
-        // ===================== MMA issuer =====================
+        // ===================== MMA issuer: S(j) and O(j) in readiness order =====================
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(kR, kT, 0, 0);
             const uint32_t id_o = idesc_bf16(kR, kHalfLat, 0, 1);
             const uint32_t q_addr = smem_u32(sQ);
-            auto issue_o = [&](int jj) -> bool {
-                const int s = jj & 1;
-                if (!wait_bounded(&pfull[s], (jj >> 1) & 1, p.status)) return false;
-                tc_fence_after();
-                const uint32_t st_addr = smem_u32(sm + kOffStage + s * kStageB);
-#pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk) {
-                    // A = P from TMEM (16 tokens = 8 packed columns per step); B = C^T: this
-                    // CTA's 256 latents (4 boxes, LBO = box stride) x 16 tokens (SBO = 8 tokens)
-                    const uint64_t bd = smem_desc(st_addr + kk * 2048, kT * 128, 1024, kSwizzle128B);
-                    mma_bf16_tmem_a(tmem + kCO, tmem + kCP + s * (kT / 2) + kk * 8, bd, id_o,
-                                    (jj > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(&empty[s]);
-                mma_commit(&pdone[s]);
-                return true;
-            };
-            bool ok = true;
-            for (int j = 0; j < n_t && ok; ++j) {
-                const int s = j & 1;
-                if (!wait_bounded(&full[s], (j >> 1) & 1, p.status)) { ok = false; break; }
-                // single S buffer: the softmax has read the previous tile's logits
-                if (j >= 1 && !wait_bounded(sfree, (j - 1) & 1, p.status)) { ok = false; break; }
+            auto issue_s = [&](int j) {
+                const int s = j % kNst;
                 tc_fence_after();
                 const uint32_t st_addr = smem_u32(sm + kOffStage + s * kStageB);
 #pragma unroll
@@ -256,9 +242,54 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                         mma_bf16(tmem + kCSr, a, bd, id_s, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(sfull);
-                if (j >= 1) ok = issue_o(j - 1);
+            };
+            auto issue_o = [&](int j) {
+                const int s = j % kNst, pb = j & 1;
+                tc_fence_after();
+                const uint32_t st_addr = smem_u32(sm + kOffStage + s * kStageB);
+#pragma unroll
+                for (int kk = 0; kk < kT / 16; ++kk) {
+                    // A = P from TMEM (16 tokens = 8 packed columns per step); B = C^T: this
+                    // CTA's 256 latents (4 boxes, LBO = box stride) x 16 tokens (SBO = 8 tokens)
+                    const uint64_t bd = smem_desc(st_addr + kk * 2048, kT * 128, 1024, kSwizzle128B);
+                    mma_bf16_tmem_a(tmem + kCO, tmem + kCP + pb * (kT / 2) + kk * 8, bd, id_o,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&empty[s]);
+                mma_commit(&pdone[pb]);
+            };
+            // every barrier below completes once per tile and is tested for its tiles in
+            // order, so each parity names exactly one phase
+            int js = 0, jo = 0;
+            uint64_t t_last = globaltimer();
+            uint32_t idle = 0;
+            bool ok = true;
+            while (jo < n_t) {
+                bool did = false;
+                // the logit MMA of tile js: the tile has landed and the softmax has read S(js-1)
+                if (js < n_t && mbar_test_wait(&full[js % kNst], (js / kNst) & 1) &&
+                    (js == 0 || mbar_test_wait(sfree, (js - 1) & 1))) {
+                    issue_s(js);
+                    ++js;
+                    did = true;
+                }
+                // the output MMA of tile jo: its P is written
+                if (jo < js && mbar_test_wait(&pfull[jo & 1], (jo >> 1) & 1)) {
+                    issue_o(jo);
+                    ++jo;
+                    did = true;
+                }
+                if (did) {
+                    idle = 0;
+                    t_last = globaltimer();
+                } else if ((++idle & 255u) == 0) {
+                    if (*(volatile int*)abort_flag || globaltimer() - t_last > kWaitNs) {
+                        report(p.status, QKMLA_ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                }
             }
-            if (ok && n_t > 0) ok = issue_o(n_t - 1);
             if (!ok) *(volatile int*)abort_flag = 1;
         }
     } else {
@@ -269,79 +300,99 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
         const int g = (r % p.H) / hpg;
         const float coef = coef_s[r];
         const float rs = p.scale * kLog2e;
-        const uint32_t my_slice = (uint32_t)sub * (kXB / 4);
+        const uint32_t my_slice = (uint32_t)sub * kXSlice;
+        uint8_t* y_row = sY + my_slice + lane * kXRow;
+        const uint8_t* x_row = sX + my_slice + lane * kXRow;
         const uint32_t peer_x = map_to_rank(smem_u32(sX) + my_slice, peer);
         const uint32_t peer_xfull = map_to_rank(smem_u32(&xfull[sub]), peer);
         const uint32_t peer_xfree = map_to_rank(smem_u32(&xfree[sub]), peer);
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        // partial logits of one tile (this CTA's half of K), scaled: S from TMEM
-        auto partial = [&](int j, float (&out)[kT]) -> bool {
-            const bool got = wait_bounded(sfull, j & 1, p.status);
+        float lg[kT];
+        for (int j = 0; j < n_t; ++j) {
+            const int s = j % kNst, pb = j & 1;
+            const int tile = jt0 + j;
+            const int valid = min(kT, L - tile * kT);
+            // ---- partial logits of this CTA's half of K, scaled ----
+            bool got = wait_bounded(sfull, j & 1, p.status);
             tc_fence_after();
-            const float* ak_t = (const float*)(sm + kOffStage + (j & 1) * kStageB + kSLat + kSRope);
+            {
+                const float* ak_t = (const float*)(sm + kOffStage + s * kStageB + kSLat + kSRope);
 #pragma unroll
-            for (int c = 0; c < kT / 32; ++c) {
-                uint32_t sc[32], sr[32];
-                tmem_ld16(tmem + kCSc + lane_base + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(sc));
-                tmem_ld16(tmem + kCSc + lane_base + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
-                if (!PLAIN) {
-                    tmem_ld16(tmem + kCSr + lane_base + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(sr));
-                    tmem_ld16(tmem + kCSr + lane_base + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(sr + 16));
-                }
-                tmem_wait_ld();
+                for (int c = 0; c < kT / 32; ++c) {
+                    uint32_t sc[32], sr[32];
+                    tmem_ld16(tmem + kCSc + lane_base + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(sc));
+                    tmem_ld16(tmem + kCSc + lane_base + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
+                    if (!PLAIN) {
+                        tmem_ld16(tmem + kCSr + lane_base + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(sr));
+                        tmem_ld16(tmem + kCSr + lane_base + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(sr + 16));
+                    }
+                    tmem_wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int t = 32 * c + jj;
-                    out[t] = PLAIN ? rs * __uint_as_float(sc[jj])
-                                   : fmaf(coef * ak_t[t * p.G + g], __uint_as_float(sc[jj]), __uint_as_float(sr[jj]));
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int t = 32 * c + jj;
+                        lg[t] = PLAIN ? rs * __uint_as_float(sc[jj])
+                                      : fmaf(coef * ak_t[t * p.G + g], __uint_as_float(sc[jj]), __uint_as_float(sr[jj]));
+                    }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(sfree);
-            return got;
-        };
-        float lg[kT];
-        for (int j = 0; j < n_t; ++j) {
-            const int s = j & 1;
-            const int tile = jt0 + j;
-            bool got = partial(j, lg);
-            // stage this tile's partial rows and send them to the other CTA
+            if (valid < kT) {
 #pragma unroll
-            for (int k = 0; k < kT / 4; ++k)
-                *reinterpret_cast<float4*>(sY + xoff(r, k)) = make_float4(lg[4 * k], lg[4 * k + 1], lg[4 * k + 2], lg[4 * k + 3]);
+                for (int t = 0; t < kT; ++t)
+                    if (t >= valid) lg[t] = -INFINITY;
+            }
+            // ---- stage (fp16, relative to the row max) and send to the other CTA ----
+            float mo[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) mo[q] = fmaxf(fmaxf(lg[q], lg[q + 8]), fmaxf(lg[q + 16], lg[q + 24]));
+#pragma unroll
+            for (int q = 0; q < 8; ++q) mo[q] = fmaxf(mo[q], fmaxf(fmaxf(lg[q + 32], lg[q + 40]), fmaxf(lg[q + 48], lg[q + 56])));
+            const float m_own = fmaxf(fmaxf(fmaxf(mo[0], mo[1]), fmaxf(mo[2], mo[3])),
+                                      fmaxf(fmaxf(mo[4], mo[5]), fmaxf(mo[6], mo[7])));
+#pragma unroll
+            for (int c8 = 0; c8 < kT / 8; ++c8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const __half2 h2 = __floats2half2_rn(lg[8 * c8 + 2 * u] - m_own, lg[8 * c8 + 2 * u + 1] - m_own);
+                    w[u] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
+                *reinterpret_cast<uint4*>(y_row + 16 * c8) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            *reinterpret_cast<float*>(y_row + 128) = m_own;
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 // the other CTA's warp has consumed the previous tile from these rows
                 const bool free_ok = (j == 0) || wait_bounded_cluster(&xfree[sub], (j - 1) & 1, p.status);
                 if (free_ok && got) {
-                    bulk_copy_to_cta(peer_x, sY + my_slice, kXB / 4, peer_xfull);
+                    bulk_copy_to_cta(peer_x, sY + my_slice, kXSlice, peer_xfull);
                     bulk_commit_group();
                 } else {
                     got = false;
                 }
             }
             got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+            // ---- full logits: own fp32 partial + the other CTA's ----
             const bool got_x = got && wait_bounded_cluster(&xfull[sub], j & 1, p.status);
             if (got_x) {
+                const float off = *reinterpret_cast<const float*>(x_row + 128);
 #pragma unroll
-                for (int k = 0; k < kT / 4; ++k) {
-                    const float4 v = *reinterpret_cast<const float4*>(sX + xoff(r, k));
-                    lg[4 * k] += v.x;
-                    lg[4 * k + 1] += v.y;
-                    lg[4 * k + 2] += v.z;
-                    lg[4 * k + 3] += v.w;
+                for (int c8 = 0; c8 < kT / 8; ++c8) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(x_row + 16 * c8);
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[u]));
+                        lg[8 * c8 + 2 * u] += off + f.x;
+                        lg[8 * c8 + 2 * u + 1] += off + f.y;
+                    }
                 }
             }
             if (!__all_sync(0xffffffffu, got_x)) { ok = false; *(volatile int*)abort_flag = 1; break; }
-            const int valid = min(kT, L - tile * kT);
-            if (valid < kT) {
-#pragma unroll
-                for (int t = 0; t < kT; ++t)
-                    if (t >= valid) lg[t] = -INFINITY;
-            }
             float mx[8];                                   // tree max: short dependency chains
 #pragma unroll
             for (int q = 0; q < 8; ++q) mx[q] = fmaxf(fmaxf(lg[q], lg[q + 8]), fmaxf(lg[q + 16], lg[q + 24]));
@@ -353,7 +404,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             // tile and let the other CTA overwrite these rows
             const float mt_w = warp_max(mt);
             if (lane == 0 && j + 1 < n_t) {
-                mbar_arrive_expect_tx(&xfull[sub], kXB / 4);
+                mbar_arrive_expect_tx(&xfull[sub], kXSlice);
                 mbar_arrive_remote_relaxed(peer_xfree, mt_w);
             }
             // lazy running max: move it only when the tile max exceeds it by > 8 (log2)
@@ -383,9 +434,9 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 tmem_wait_st();
             }
             l_run *= corr;
-            // P (bf16) into TMEM buffer s once the output MMA two tiles back released it
+            // P (bf16) into TMEM buffer pb once the output MMA two tiles back released it
             if (j >= 2) {
-                const bool got_p = wait_bounded(&pdone[s], ((j >> 1) - 1) & 1, p.status);
+                const bool got_p = wait_bounded(&pdone[pb], ((j >> 1) - 1) & 1, p.status);
                 if (!__all_sync(0xffffffffu, got_p)) { ok = false; *(volatile int*)abort_flag = 1; break; }
                 tc_fence_after();
             }
@@ -401,7 +452,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                     const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
                     w16[q] = *reinterpret_cast<const uint32_t*>(&b2);
                 }
-                tmem_st16(tmem + kCP + s * (kT / 2) + 16 * h + lane_base, w16);
+                tmem_st16(tmem + kCP + pb * (kT / 2) + 16 * h + lane_base, w16);
             }
             tmem_wait_st();
             l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
@@ -418,7 +469,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&pfull[s]);
+                mbar_arrive(&pfull[pb]);
                 bulk_wait_read_all();       // Y may be restaged for the next tile
             }
             __syncwarp();
