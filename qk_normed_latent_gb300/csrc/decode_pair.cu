@@ -50,7 +50,7 @@ constexpr int kR = 128;            // query rows per pair
 constexpr int kDC = 512, kDR = 64;
 constexpr int kHalfLat = kDC / 2;  // latent columns per CTA
 constexpr int kHalfRope = kDR / 2; // RoPE columns per CTA
-constexpr int kThreadsP = 192;
+constexpr int kThreadsP = 320;    // 2 + 4 + 4 warps
 constexpr int kNst = 3;            // TMA stages
 
 // shared memory (offsets from a 1024-byte aligned base)
@@ -60,25 +60,27 @@ constexpr int kSLat = 4 * kT * 128;                    // tile half: 4 boxes of 
 constexpr int kSRope = kT * 64;                        // 64 tokens x 64 B
 constexpr int kSAk = kT * kMaxG * 4;
 constexpr int kStageB = kSLat + kSRope + kSAk;         // 38 KB
-// exchange row: 64 fp16 partial logits minus the row maximum (128 B), the
-// maximum (fp32), padding to 144 B (conflict-free 16-byte accesses by 32 rows)
-constexpr int kXRow = 144;
-constexpr int kXSlice = 32 * kXRow;                    // one softmax warp's 32 rows
+// exchange slice of one row group: 32 rows x 64 fp16 partial logits minus the
+// row's maximum (128-byte rows, 16-byte chunks XOR-swizzled by row), then the
+// 32 maxima (fp32)
+constexpr int kXRowB = kT * 2;
+constexpr int kXSlice = 32 * kXRowB + 32 * 4;
 constexpr int kXB = 4 * kXSlice;
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kQLat + kQRope;
 constexpr int kOffX = kOffStage + kNst * kStageB;      // received partials
 constexpr int kOffY = kOffX + kXB;                     // own partials (sent)
 constexpr int kOffMisc = kOffY + kXB;
-constexpr int kNumBars = 20;
+constexpr int kNumBars = 22;
 constexpr int kBytesP = kOffMisc + kNumBars * 8 + 16 + kR * 4 + 1024;
 static_assert(kStageB % 1024 == 0 && kOffStage % 1024 == 0 && kOffX % 16 == 0 && kOffY % 16 == 0, "align");
 static_assert(kXSlice % 16 == 0, "bulk copy size");
 static_assert(kBytesP <= 232448, "shared memory budget");
 
 // TMEM columns: S_c at 0, S_r at 64, P[2] (64 bf16 tokens = 32 columns each) at
-// 128 / 160, O (128 rows x 256 latents) at 256
-constexpr uint32_t kCSc = 0, kCSr = 64, kCP = 128, kCO = 256;
+// 128 / 160, this CTA's scaled partial logits (fp32, parked by group A for group
+// B) at 192, O (128 rows x 256 latents) at 256
+constexpr uint32_t kCSc = 0, kCSr = 64, kCP = 128, kCOwn = 192, kCO = 256;
 
 template <bool PLAIN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsP, 1)
@@ -98,6 +100,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     uint64_t* pfull = bars + 10;    // [2] P written -> output MMA
     uint64_t* xfull = bars + 12;    // [4] per warp: the other CTA's partial rows landed in X
     uint64_t* xfree = bars + 16;    // [4] per warp: the other CTA's X rows may be overwritten
+    uint64_t* ownfull = bars + 20;  // group A parked a tile's partials -> group B
+    uint64_t* ownfree = bars + 21;  // group B read them -> group A
     uint32_t* tmem_slot = (uint32_t*)(bars + kNumBars);
     int* abort_flag = (int*)(tmem_slot + 1);
     float* coef_s = (float*)(sm + kOffMisc + kNumBars * 8 + 16);
@@ -122,7 +126,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     if (tid == 0) {
         if (bad && rank == 0) report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
         for (int i = 0; i < kNumBars; ++i) {
-            const bool four = (i == 7 || i == 10 || i == 11);   // sfree, pfull: one per softmax warp
+            const bool four = (i == 7 || i == 10 || i == 11 || i == 20 || i == 21);   // one per warp of a group
             mbar_init(&bars[i], four ? 4u : 1u);
         }
         *abort_flag = 0;
@@ -138,12 +142,12 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     if (warp >= 2) {
         const int st = tid - 64;
         const size_t qrow0 = ((size_t)b * p.s_q + qi) * p.H;
-        for (int e = st; e < kR * (kHalfLat / 8); e += 128) {
+        for (int e = st; e < kR * (kHalfLat / 8); e += 256) {
             const int r = e / (kHalfLat / 8), k = e % (kHalfLat / 8);    // k: 16-byte chunk in the half row
             const uint4 v = *reinterpret_cast<const uint4*>(p.qt + (qrow0 + r) * kDC + rank * kHalfLat + k * 8);
             *reinterpret_cast<uint4*>(sQ + (k >> 3) * (kR * 128) + sw128_offset(r, (k & 7) * 8)) = v;
         }
-        {   // one thread per row: RMS over all 64 RoPE dims, keep this CTA's 32
+        if (st < kR) {   // one thread per row: RMS over all 64 RoPE dims, keep this CTA's 32
             const int r = st;
             const float* src = p.qr + (qrow0 + r) * kDR;
             float ss = 0.f;
@@ -164,7 +168,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             coef_s[r] = PLAIN ? 0.f : p.scale * p.aq[qrow0 + r] * kLog2e;
         }
         fence_proxy_async_smem();
-        if (lane == 0 && n_t > 0) mbar_arrive_expect_tx(&xfull[warp & 3], kXSlice);   // tile 0's rows
+        if (warp >= 6 && lane == 0 && n_t > 0) mbar_arrive_expect_tx(&xfull[warp & 3], kXSlice);   // tile 0's rows
     }
     tc_fence_before();
     cluster_sync();            // both CTAs' barriers exist before any remote access
@@ -293,237 +297,279 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             if (!ok) *(volatile int*)abort_flag = 1;
         }
     } else {
-        // ===================== softmax / exchange / epilogue: thread = query row =====================
+        // ===================== softmax: two groups of four warps, thread = query row =====================
+        // Group A (warps 2-5) turns S(j) into this CTA's scaled partial logits, parks
+        // them in TMEM (scratch columns) and sends them (fp16) to the other CTA; group
+        // B (warps 6-9) adds the other CTA's partials, runs the online softmax and
+        // writes P.  A works on tile j+1 while B finishes tile j.
         const int sub = warp & 3;                        // TMEM sub-partition = exchange slice
+        const bool grp_a = warp < 6;
         const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
         const int r = 32 * sub + lane;                   // M=128 accumulator: row r in TMEM lane r
-        const int g = (r % p.H) / hpg;
-        const float coef = coef_s[r];
-        const float rs = p.scale * kLog2e;
         const uint32_t my_slice = (uint32_t)sub * kXSlice;
-        uint8_t* y_row = sY + my_slice + lane * kXRow;
-        const uint8_t* x_row = sX + my_slice + lane * kXRow;
-        const uint32_t peer_x = map_to_rank(smem_u32(sX) + my_slice, peer);
-        const uint32_t peer_xfull = map_to_rank(smem_u32(&xfull[sub]), peer);
-        const uint32_t peer_xfree = map_to_rank(smem_u32(&xfree[sub]), peer);
-        float m_run = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        float lg[kT];
-        for (int j = 0; j < n_t; ++j) {
-            const int s = j % kNst, pb = j & 1;
-            const int tile = jt0 + j;
-            const int valid = min(kT, L - tile * kT);
-            // ---- partial logits of this CTA's half of K, scaled ----
-            bool got = wait_bounded(sfull, j & 1, p.status);
-            tc_fence_after();
-            {
+        const uint32_t xrow = my_slice + lane * kXRowB;  // this row's 128 fp16 bytes in a slice
+        float* const x_off = reinterpret_cast<float*>(sX + my_slice + 32 * kXRowB);   // 32 maxima
+        float* const y_off = reinterpret_cast<float*>(sY + my_slice + 32 * kXRowB);
+        if (grp_a) {
+            const int g = (r % p.H) / hpg;
+            const float coef = coef_s[r];
+            const float rs = p.scale * kLog2e;
+            const uint32_t peer_x = map_to_rank(smem_u32(sX) + my_slice, peer);
+            const uint32_t peer_xfull = map_to_rank(smem_u32(&xfull[sub]), peer);
+            float pv[kT];
+            for (int j = 0; j < n_t; ++j) {
+                const int s = j % kNst;
+                const int valid = min(kT, L - (jt0 + j) * kT);
+                const bool got_s = __all_sync(0xffffffffu, wait_bounded(sfull, j & 1, p.status));
+                tc_fence_after();
                 const float* ak_t = (const float*)(sm + kOffStage + s * kStageB + kSLat + kSRope);
 #pragma unroll
-                for (int c = 0; c < kT / 32; ++c) {
-                    uint32_t sc[32], sr[32];
-                    tmem_ld16(tmem + kCSc + lane_base + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(sc));
-                    tmem_ld16(tmem + kCSc + lane_base + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(sc + 16));
-                    if (!PLAIN) {
-                        tmem_ld16(tmem + kCSr + lane_base + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(sr));
-                        tmem_ld16(tmem + kCSr + lane_base + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(sr + 16));
-                    }
+                for (int c = 0; c < kT / 16; ++c) {
+                    uint32_t sc[16], sr[16];
+                    tmem_ld16(tmem + kCSc + lane_base + 16 * c, sc);
+                    if (!PLAIN) tmem_ld16(tmem + kCSr + lane_base + 16 * c, sr);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int t = 32 * c + jj;
-                        lg[t] = PLAIN ? rs * __uint_as_float(sc[jj])
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int t = 16 * c + jj;
+                        pv[t] = PLAIN ? rs * __uint_as_float(sc[jj])
                                       : fmaf(coef * ak_t[t * p.G + g], __uint_as_float(sc[jj]), __uint_as_float(sr[jj]));
                     }
                 }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sfree);
-            if (valid < kT) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sfree);
+                if (valid < kT) {
 #pragma unroll
-                for (int t = 0; t < kT; ++t)
-                    if (t >= valid) lg[t] = -INFINITY;
-            }
-            // ---- stage (fp16, relative to the row max) and send to the other CTA ----
-            float mo[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) mo[q] = fmaxf(fmaxf(lg[q], lg[q + 8]), fmaxf(lg[q + 16], lg[q + 24]));
-#pragma unroll
-            for (int q = 0; q < 8; ++q) mo[q] = fmaxf(mo[q], fmaxf(fmaxf(lg[q + 32], lg[q + 40]), fmaxf(lg[q + 48], lg[q + 56])));
-            const float m_own = fmaxf(fmaxf(fmaxf(mo[0], mo[1]), fmaxf(mo[2], mo[3])),
-                                      fmaxf(fmaxf(mo[4], mo[5]), fmaxf(mo[6], mo[7])));
-#pragma unroll
-            for (int c8 = 0; c8 < kT / 8; ++c8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const __half2 h2 = __floats2half2_rn(lg[8 * c8 + 2 * u] - m_own, lg[8 * c8 + 2 * u + 1] - m_own);
-                    w[u] = *reinterpret_cast<const uint32_t*>(&h2);
+                    for (int t = 0; t < kT; ++t)
+                        if (t >= valid) pv[t] = -INFINITY;
                 }
-                *reinterpret_cast<uint4*>(y_row + 16 * c8) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            *reinterpret_cast<float*>(y_row + 128) = m_own;
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                // the other CTA's warp has consumed the previous tile from these rows
-                const bool free_ok = (j == 0) || wait_bounded_cluster(&xfree[sub], (j - 1) & 1, p.status);
-                if (free_ok && got) {
-                    bulk_copy_to_cta(peer_x, sY + my_slice, kXSlice, peer_xfull);
-                    bulk_commit_group();
-                } else {
-                    got = false;
-                }
-            }
-            got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-            // ---- full logits: own fp32 partial + the other CTA's ----
-            const bool got_x = got && wait_bounded_cluster(&xfull[sub], j & 1, p.status);
-            if (got_x) {
-                const float off = *reinterpret_cast<const float*>(x_row + 128);
-#pragma unroll
-                for (int c8 = 0; c8 < kT / 8; ++c8) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(x_row + 16 * c8);
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[u]));
-                        lg[8 * c8 + 2 * u] += off + f.x;
-                        lg[8 * c8 + 2 * u + 1] += off + f.y;
-                    }
-                }
-            }
-            if (!__all_sync(0xffffffffu, got_x)) { ok = false; *(volatile int*)abort_flag = 1; break; }
-            float mx[8];                                   // tree max: short dependency chains
-#pragma unroll
-            for (int q = 0; q < 8; ++q) mx[q] = fmaxf(fmaxf(lg[q], lg[q + 8]), fmaxf(lg[q + 16], lg[q + 24]));
-#pragma unroll
-            for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], fmaxf(fmaxf(lg[q + 32], lg[q + 40]), fmaxf(lg[q + 48], lg[q + 56])));
-            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            // every X value has been read (mt depends on all of them): arm for the next
-            // tile and let the other CTA overwrite these rows
-            const float mt_w = warp_max(mt);
-            if (lane == 0 && j + 1 < n_t) {
-                mbar_arrive_expect_tx(&xfull[sub], kXSlice);
-                mbar_arrive_remote_relaxed(peer_xfree, mt_w);
-            }
-            // lazy running max: move it only when the tile max exceeds it by > 8 (log2)
-            float corr = 1.f;
-            const bool need = mt > m_run + 8.f;
-            if (need) {
-                corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mt);
-                m_run = mt;
-            }
-            // TMEM loads/stores are warp-collective: the whole warp rescales when any
-            // of its rows needs it, each lane by its own factor (1 for the others)
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
-                // the previous tile's output MMA: its P buffer's barrier, whose earlier
-                // phases this warp has consumed (so the parity names one phase)
-                const bool got_o = wait_bounded(&pdone[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status);
-                if (!__all_sync(0xffffffffu, got_o)) { ok = false; *(volatile int*)abort_flag = 1; break; }
+                // park the fp32 partials for group B once it has read the previous ones
+                bool ok_a = got_s;
+                if (j >= 1) ok_a = __all_sync(0xffffffffu, wait_bounded(ownfree, (j - 1) & 1, p.status)) && ok_a;
                 tc_fence_after();
-#pragma unroll 1
-                for (int c16 = 0; c16 < kHalfLat; c16 += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tmem + kCO + c16 + lane_base, v);
-                    tmem_wait_ld();
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) * corr);
-                    tmem_st16(tmem + kCO + c16 + lane_base, v);
+                for (int q = 0; q < kT / 16; ++q) {
+                    uint32_t w16[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) w16[jj] = __float_as_uint(pv[16 * q + jj]);
+                    tmem_st16(tmem + kCOwn + lane_base + 16 * q, w16);
                 }
                 tmem_wait_st();
-            }
-            l_run *= corr;
-            // P (bf16) into TMEM buffer pb once the output MMA two tiles back released it
-            if (j >= 2) {
-                const bool got_p = wait_bounded(&pdone[pb], ((j >> 1) - 1) & 1, p.status);
-                if (!__all_sync(0xffffffffu, got_p)) { ok = false; *(volatile int*)abort_flag = 1; break; }
-                tc_fence_after();
-            }
-            float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+                // stage fp16 relative to the row max, once the previous send has read Y
+                float mo[8];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t w16[16];
+                for (int q = 0; q < 8; ++q) mo[q] = fmaxf(fmaxf(pv[q], pv[q + 8]), fmaxf(pv[q + 16], pv[q + 24]));
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float e0 = fast_exp2(lg[32 * h + 2 * q] - m_run);
-                    const float e1 = fast_exp2(lg[32 * h + 2 * q + 1] - m_run);
-                    ps4[q & 3] += e0 + e1;
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
-                    w16[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                for (int q = 0; q < 8; ++q) mo[q] = fmaxf(mo[q], fmaxf(fmaxf(pv[q + 32], pv[q + 40]), fmaxf(pv[q + 48], pv[q + 56])));
+                const float m_own = fmaxf(fmaxf(fmaxf(mo[0], mo[1]), fmaxf(mo[2], mo[3])),
+                                          fmaxf(fmaxf(mo[4], mo[5]), fmaxf(mo[6], mo[7])));
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+#pragma unroll
+                for (int c8 = 0; c8 < kT / 8; ++c8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const __half2 h2 = __floats2half2_rn(pv[8 * c8 + 2 * u] - m_own, pv[8 * c8 + 2 * u + 1] - m_own);
+                        w[u] = *reinterpret_cast<const uint32_t*>(&h2);
+                    }
+                    *reinterpret_cast<uint4*>(sY + xrow + ((c8 ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                tmem_st16(tmem + kCP + pb * (kT / 2) + 16 * h + lane_base, w16);
-            }
-            tmem_wait_st();
-            l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-            if (valid < kT) {   // zero this CTA's latent rows past the sequence end (this warp's share)
-                uint8_t* stg = sm + kOffStage + s * kStageB;
-                const int nrow = kT - valid;
-                for (int e = lane + 32 * sub; e < nrow * 4 * 8; e += 128) {
-                    const int rr = valid + e / 32, rem = e % 32;
-                    *reinterpret_cast<uint4*>(stg + (rem >> 3) * (kT * 128) + rr * 128 + (rem & 7) * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
+                y_off[lane] = m_own;
                 fence_proxy_async_smem();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&pfull[pb]);
-                bulk_wait_read_all();       // Y may be restaged for the next tile
-            }
-            __syncwarp();
-        }
-        // ---- epilogue: thread = row, its 256 latents ----
-        bool got_last =
-            (ok && n_t > 0) ? wait_bounded(&pdone[(n_t - 1) & 1], ((n_t - 1) >> 1) & 1, p.status) : true;
-        got_last = __all_sync(0xffffffffu, got_last);      // TMEM reads below are warp-collective
-        tc_fence_after();
-        if (!got_last) *(volatile int*)abort_flag = 1;
-        const size_t orow = ((size_t)b * p.s_q + qi) * p.H + r;
-        if (rank == 0) {
-            const float lse = (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-            if (it.part < 0) {
-                if (p.lse) p.lse[orow] = lse;
-            } else {
-                p.lse_part[(size_t)it.part * p.s_q * p.H + (size_t)qi * p.H + r] = lse;
-            }
-        }
-        const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-        float* dst_part = (it.part >= 0)
-                              ? p.o_part + ((size_t)it.part * p.s_q * p.H + (size_t)qi * p.H + r) * kDC + rank * kHalfLat
-                              : nullptr;
-#pragma unroll 1
-        for (int c16 = 0; c16 < kHalfLat; c16 += 16) {
-            uint32_t v[16];
-            if (n_t > 0 && got_last) {
-                tmem_ld16(tmem + kCO + c16 + lane_base, v);
-                tmem_wait_ld();
-            } else {
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) v[jj] = 0u;
-            }
-            float o16[16];
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) o16[jj] = __uint_as_float(v[jj]) * inv;
-            if (dst_part) {
-                float4* d4 = reinterpret_cast<float4*>(dst_part + c16);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) d4[q] = make_float4(o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
-            } else if (p.o_dtype == QKMLA_F32) {
-                float4* d4 = reinterpret_cast<float4*>((float*)p.o + orow * kDC + rank * kHalfLat + c16);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) d4[q] = make_float4(o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
-            } else {
-                uint32_t w[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(o16[2 * q], o16[2 * q + 1]);
-                    w[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                __syncwarp();
+                if (lane == 0) {
+                    // the other CTA's group B has consumed the previous tile from these rows
+                    if (ok_a && j >= 1) ok_a = wait_bounded_cluster(&xfree[sub], (j - 1) & 1, p.status);
+                    if (ok_a) {
+                        bulk_copy_to_cta(peer_x, sY + my_slice, kXSlice, peer_xfull);
+                        bulk_commit_group();
+                    }
                 }
-                uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)p.o + orow * kDC + rank * kHalfLat + c16);
-                d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                ok_a = __shfl_sync(0xffffffffu, ok_a ? 1 : 0, 0) != 0;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ownfull);
+                if (!ok_a) { *(volatile int*)abort_flag = 1; break; }
+            }
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+        } else {
+            const uint32_t peer_xfree = map_to_rank(smem_u32(&xfree[sub]), peer);
+            float m_run = -INFINITY, l_run = 0.f;
+            bool ok = true;
+            float lg[kT];
+            for (int j = 0; j < n_t; ++j) {
+                const int s = j % kNst, pb = j & 1;
+                const int valid = min(kT, L - (jt0 + j) * kT);
+                // ---- this CTA's fp32 partials from group A ----
+                const bool got_own = __all_sync(0xffffffffu, wait_bounded(ownfull, j & 1, p.status));
+                tc_fence_after();
+                {
+                    uint32_t v[kT];
+#pragma unroll
+                    for (int q = 0; q < kT / 16; ++q)
+                        tmem_ld16(tmem + kCOwn + lane_base + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * q));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int t = 0; t < kT; ++t) lg[t] = __uint_as_float(v[t]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ownfree);
+                // ---- + the other CTA's ----
+                const bool got_x =
+                    __all_sync(0xffffffffu, got_own && wait_bounded_cluster(&xfull[sub], j & 1, p.status));
+                if (got_x) {
+                    const float off = x_off[lane];
+#pragma unroll
+                    for (int c8 = 0; c8 < kT / 8; ++c8) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(sX + xrow + ((c8 ^ (lane & 7)) << 4));
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[u]));
+                            lg[8 * c8 + 2 * u] += off + f.x;
+                            lg[8 * c8 + 2 * u + 1] += off + f.y;
+                        }
+                    }
+                }
+                if (!got_x) { ok = false; *(volatile int*)abort_flag = 1; break; }
+                if (valid < kT) {
+#pragma unroll
+                    for (int t = 0; t < kT; ++t)
+                        if (t >= valid) lg[t] = -INFINITY;
+                }
+                float mx[8];                                   // tree max: short dependency chains
+#pragma unroll
+                for (int q = 0; q < 8; ++q) mx[q] = fmaxf(fmaxf(lg[q], lg[q + 8]), fmaxf(lg[q + 16], lg[q + 24]));
+#pragma unroll
+                for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], fmaxf(fmaxf(lg[q + 32], lg[q + 40]), fmaxf(lg[q + 48], lg[q + 56])));
+                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                // every X value has been read (mt depends on all of them): arm for the next
+                // tile and let the other CTA overwrite these rows
+                const float mt_w = warp_max(mt);
+                if (lane == 0 && j + 1 < n_t) {
+                    mbar_arrive_expect_tx(&xfull[sub], kXSlice);
+                    mbar_arrive_remote_relaxed(peer_xfree, mt_w);
+                }
+                // lazy running max: move it only when the tile max exceeds it by > 8 (log2)
+                float corr = 1.f;
+                const bool need = mt > m_run + 8.f;
+                if (need) {
+                    corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mt);
+                    m_run = mt;
+                }
+                // TMEM loads/stores are warp-collective: the whole warp rescales when any
+                // of its rows needs it, each lane by its own factor (1 for the others)
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                    // the previous tile's output MMA: its P buffer's barrier, whose earlier
+                    // phases this warp has consumed (so the parity names one phase)
+                    const bool got_o =
+                        __all_sync(0xffffffffu, wait_bounded(&pdone[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status));
+                    if (!got_o) { ok = false; *(volatile int*)abort_flag = 1; break; }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c16 = 0; c16 < kHalfLat; c16 += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(tmem + kCO + c16 + lane_base, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) * corr);
+                        tmem_st16(tmem + kCO + c16 + lane_base, v);
+                    }
+                    tmem_wait_st();
+                }
+                l_run *= corr;
+                // P (bf16) into TMEM buffer pb once the output MMA two tiles back released it
+                if (j >= 2) {
+                    const bool got_p = __all_sync(0xffffffffu, wait_bounded(&pdone[pb], ((j >> 1) - 1) & 1, p.status));
+                    if (!got_p) { ok = false; *(volatile int*)abort_flag = 1; break; }
+                    tc_fence_after();
+                }
+                float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t w16[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const float e0 = fast_exp2(lg[32 * h + 2 * q] - m_run);
+                        const float e1 = fast_exp2(lg[32 * h + 2 * q + 1] - m_run);
+                        ps4[q & 3] += e0 + e1;
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
+                        w16[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                    }
+                    tmem_st16(tmem + kCP + pb * (kT / 2) + 16 * h + lane_base, w16);
+                }
+                tmem_wait_st();
+                l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+                if (valid < kT) {   // zero this CTA's latent rows past the sequence end (this warp's share)
+                    uint8_t* stg = sm + kOffStage + s * kStageB;
+                    const int nrow = kT - valid;
+                    for (int e = lane + 32 * sub; e < nrow * 4 * 8; e += 128) {
+                        const int rr = valid + e / 32, rem = e % 32;
+                        *reinterpret_cast<uint4*>(stg + (rem >> 3) * (kT * 128) + rr * 128 + (rem & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&pfull[pb]);
+            }
+            // ---- epilogue: thread = row, its 256 latents ----
+            bool got_last =
+                (ok && n_t > 0) ? wait_bounded(&pdone[(n_t - 1) & 1], ((n_t - 1) >> 1) & 1, p.status) : true;
+            got_last = __all_sync(0xffffffffu, got_last);      // TMEM reads below are warp-collective
+            tc_fence_after();
+            if (!got_last) *(volatile int*)abort_flag = 1;
+            const size_t orow = ((size_t)b * p.s_q + qi) * p.H + r;
+            if (rank == 0) {
+                const float lse = (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+                if (it.part < 0) {
+                    if (p.lse) p.lse[orow] = lse;
+                } else {
+                    p.lse_part[(size_t)it.part * p.s_q * p.H + (size_t)qi * p.H + r] = lse;
+                }
+            }
+            const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+            float* dst_part = (it.part >= 0)
+                                  ? p.o_part + ((size_t)it.part * p.s_q * p.H + (size_t)qi * p.H + r) * kDC + rank * kHalfLat
+                                  : nullptr;
+#pragma unroll 1
+            for (int c16 = 0; c16 < kHalfLat; c16 += 16) {
+                uint32_t v[16];
+                if (n_t > 0 && got_last) {
+                    tmem_ld16(tmem + kCO + c16 + lane_base, v);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) v[jj] = 0u;
+                }
+                float o16[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) o16[jj] = __uint_as_float(v[jj]) * inv;
+                if (dst_part) {
+                    float4* d4 = reinterpret_cast<float4*>(dst_part + c16);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) d4[q] = make_float4(o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
+                } else if (p.o_dtype == QKMLA_F32) {
+                    float4* d4 = reinterpret_cast<float4*>((float*)p.o + orow * kDC + rank * kHalfLat + c16);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) d4[q] = make_float4(o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
+                } else {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(o16[2 * q], o16[2 * q + 1]);
+                        w[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                    }
+                    uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)p.o + orow * kDC + rank * kHalfLat + c16);
+                    d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                }
             }
         }
     }
