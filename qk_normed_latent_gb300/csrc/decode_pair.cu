@@ -71,7 +71,7 @@ constexpr int kOffStage = kQLat + kQRope;
 constexpr int kOffX = kOffStage + kNst * kStageB;      // received partials
 constexpr int kOffY = kOffX + kXB;                     // own partials (sent)
 constexpr int kOffMisc = kOffY + kXB;
-constexpr int kNumBars = 22;
+constexpr int kNumBars = 23;
 constexpr int kBytesP = kOffMisc + kNumBars * 8 + 16 + kR * 4 + 1024;
 static_assert(kStageB % 1024 == 0 && kOffStage % 1024 == 0 && kOffX % 16 == 0 && kOffY % 16 == 0, "align");
 static_assert(kXSlice % 16 == 0, "bulk copy size");
@@ -85,7 +85,7 @@ constexpr uint32_t kCSc = 0, kCSr = 64, kCP = 128, kCOwn = 192, kCO = 256;
 template <bool PLAIN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsP, 1)
 decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tm_q, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     uint8_t* sQ = sm + kOffQ;
@@ -102,6 +102,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     uint64_t* xfree = bars + 16;    // [4] per warp: the other CTA's X rows may be overwritten
     uint64_t* ownfull = bars + 20;  // group A parked a tile's partials -> group B
     uint64_t* ownfree = bars + 21;  // group B read them -> group A
+    uint64_t* qfull = bars + 22;    // this CTA's half of Q~ landed
     uint32_t* tmem_slot = (uint32_t*)(bars + kNumBars);
     int* abort_flag = (int*)(tmem_slot + 1);
     float* coef_s = (float*)(sm + kOffMisc + kNumBars * 8 + 16);
@@ -133,20 +134,17 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
         fence_barrier_init();
         prefetch_tmap(&tm_lat);
         prefetch_tmap(&tm_rope);
+        prefetch_tmap(&tm_q);
     }
     if (warp == 0) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
-    // ---- prologue: this CTA's half of Q~ and of the normalised RoPE query ----
+    // ---- prologue: this CTA's half of Q~ (TMA, four 64-column boxes) and of the
+    //      normalised RoPE query ----
+    const size_t qrow0 = ((size_t)b * p.s_q + qi) * p.H;
     if (warp >= 2) {
         const int st = tid - 64;
-        const size_t qrow0 = ((size_t)b * p.s_q + qi) * p.H;
-        for (int e = st; e < kR * (kHalfLat / 8); e += 256) {
-            const int r = e / (kHalfLat / 8), k = e % (kHalfLat / 8);    // k: 16-byte chunk in the half row
-            const uint4 v = *reinterpret_cast<const uint4*>(p.qt + (qrow0 + r) * kDC + rank * kHalfLat + k * 8);
-            *reinterpret_cast<uint4*>(sQ + (k >> 3) * (kR * 128) + sw128_offset(r, (k & 7) * 8)) = v;
-        }
         if (st < kR) {   // one thread per row: RMS over all 64 RoPE dims, keep this CTA's 32
             const int r = st;
             const float* src = p.qr + (qrow0 + r) * kDR;
@@ -168,12 +166,19 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             coef_s[r] = PLAIN ? 0.f : p.scale * p.aq[qrow0 + r] * kLog2e;
         }
         fence_proxy_async_smem();
-        if (warp >= 6 && lane == 0 && n_t > 0) mbar_arrive_expect_tx(&xfull[warp & 3], kXSlice);   // tile 0's rows
     }
+    // no barrier is touched before this point: thread 0's mbarrier.init must be
+    // ordered before every arrive, local or remote
     tc_fence_before();
     cluster_sync();            // both CTAs' barriers exist before any remote access
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(qfull, (uint32_t)(4 * kR * 128));
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk)
+            tma_load_2d(sQ + blk * (kR * 128), &tm_q, rank * kHalfLat + blk * 64, (int)qrow0, qfull);
+    }
 
     if (warp == 0) {
         // ===================== TMA producer: this CTA's half of each tile =====================
@@ -263,12 +268,13 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 mma_commit(&pdone[pb]);
             };
             // every barrier below completes once per tile and is tested for its tiles in
-            // order, so each parity names exactly one phase
+            // order, so each parity names exactly one phase.  Q~ is always waited for,
+            // so no CTA exits with its copy in flight.
             int js = 0, jo = 0;
+            bool ok = wait_bounded(qfull, 0, p.status);
             uint64_t t_last = globaltimer();
             uint32_t idle = 0;
-            bool ok = true;
-            while (jo < n_t) {
+            while (ok && jo < n_t) {
                 bool did = false;
                 // the logit MMA of tile js: the tile has landed and the softmax has read S(js-1)
                 if (js < n_t && mbar_test_wait(&full[js % kNst], (js / kNst) & 1) &&
@@ -397,6 +403,9 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             __syncwarp();
         } else {
             const uint32_t peer_xfree = map_to_rank(smem_u32(&xfree[sub]), peer);
+            // arm for tile 0's rows; the other CTA's copy may complete its bytes first
+            // (the transaction count goes negative), the phase still needs this arrive
+            if (lane == 0 && n_t > 0) mbar_arrive_expect_tx(&xfull[sub], kXSlice);
             float m_run = -INFINITY, l_run = 0.f;
             bool ok = true;
             float lg[kT];
@@ -586,16 +595,18 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
 }  // namespace
 
 int launch_pair(const qkmla_decode_args* a, const TcParams& tp, int max_items, cudaStream_t s) {
-    CUtensorMap lat, rope;
+    CUtensorMap lat, rope, qmap;
     const int row = a->d_c + a->d_r;
     if (!make_map(&lat, a->kv_cache, a->num_slots, row, 64, kT, CU_TENSOR_MAP_SWIZZLE_128B)) return QKMLA_ERR_CUDA;
     if (!make_map(&rope, a->kv_cache, a->num_slots, row, 32, kT, CU_TENSOR_MAP_SWIZZLE_64B)) return QKMLA_ERR_CUDA;
+    if (!make_map(&qmap, a->q_tilde, (int64_t)a->B * a->s_q * a->H, kDC, 64, kR, CU_TENSOR_MAP_SWIZZLE_128B))
+        return QKMLA_ERR_CUDA;
     const bool plain = (a->flags & QKMLA_FLAG_PLAIN_MLA) != 0;
     auto k = plain ? decode_pair_kernel<true> : decode_pair_kernel<false>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytesP) != cudaSuccess)
         return QKMLA_ERR_CUDA;
     dim3 grid(2 * a->s_q, max_items);
-    return launch_pdl(k, grid, dim3(kThreadsP), kBytesP, s, lat, rope, tp) == cudaSuccess ? QKMLA_OK
+    return launch_pdl(k, grid, dim3(kThreadsP), kBytesP, s, lat, rope, qmap, tp) == cudaSuccess ? QKMLA_OK
                                                                                        : QKMLA_ERR_CUDA;
 }
 

@@ -28,6 +28,8 @@
 // range); long sequences are split and merged afterwards by a combine kernel.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "decode_common.cuh"
 #include "tc_ptx.cuh"
@@ -536,12 +538,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
 __global__ void __launch_bounds__(1024)
 sched_kernel(const int32_t* __restrict__ seq_lens, int B, int s_q, int max_len, int n_rb, int sms, int min_tokens,
              int tile, int fixed_splits, WorkItem* __restrict__ items, int* __restrict__ n_items, int* __restrict__ seq_nsplit,
-             int* __restrict__ seq_part0, int* status) {
+             int* __restrict__ seq_part0, int* __restrict__ split_list, int* status) {
     __shared__ int tiles_s[kMaxB];
     __shared__ int ns_by_rank[kMaxB];
     __shared__ int rank_s[kMaxB];
     __shared__ int red[32];
-    __shared__ int s_total, s_tpi;
+    __shared__ int s_total, s_tpi, s_nsplit;
     const int tid = threadIdx.x, nt = blockDim.x;
     pdl_wait();
     pdl_trigger();
@@ -569,6 +571,7 @@ sched_kernel(const int32_t* __restrict__ seq_lens, int B, int s_q, int max_len, 
         int t = 0;
         for (int w = 0; w < (nt + 31) / 32; ++w) t += red[w];
         s_total = t;
+        s_nsplit = 0;
     }
     __syncthreads();
     if ((tid & 31) == 0) red[tid >> 5] = mx;
@@ -613,6 +616,7 @@ sched_kernel(const int32_t* __restrict__ seq_lens, int B, int s_q, int max_len, 
         const int off = ns_by_rank[rank_s[b]];
         seq_nsplit[b] = ns;
         seq_part0[b] = off;
+        if (ns > 1) split_list[atomicAdd(&s_nsplit, 1)] = b;   // sequences the combine visits
         for (int k = 0; k < ns; ++k) {
             WorkItem w;
             w.b = b;
@@ -622,77 +626,85 @@ sched_kernel(const int32_t* __restrict__ seq_lens, int B, int s_q, int max_len, 
             items[off + k] = w;
         }
     }
+    __syncthreads();
+    if (tid == 0) n_items[1] = s_nsplit;
 }
 
 // ---------------------------------------------------------------------------
 // combine for variable split counts
 // ---------------------------------------------------------------------------
+// A fixed grid walks the rows of the sequences the scheduler split (a compact
+// list it wrote): with no split sequence every CTA reads one count and exits.
 __global__ void __launch_bounds__(128)
 combine_var_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                   const int* __restrict__ seq_nsplit, const int* __restrict__ seq_part0, int rows_per_seq, int d_c,
+                   const int* __restrict__ seq_nsplit, const int* __restrict__ seq_part0,
+                   const int* __restrict__ split_list, const int* __restrict__ n_split, int rows_per_seq, int d_c,
                    void* __restrict__ o, int o_dtype, float* __restrict__ lse) {
     __shared__ float w_s[256];
     __shared__ float s_inv, s_lse;
-    const int row = blockIdx.x;                 // (b, i, h)
-    const int b = row / rows_per_seq, rr = row % rows_per_seq;
     pdl_wait();
     pdl_trigger();
-    const int ns = seq_nsplit[b];
-    if (ns <= 1) return;
-    const int p0 = seq_part0[b];
+    const int tasks = *n_split * rows_per_seq;
     const int tid = threadIdx.x;
-    if (tid < 32) {
-        float m = -INFINITY;
-        for (int s = tid; s < ns; s += 32) m = fmaxf(m, lse_part[(size_t)(p0 + s) * rows_per_seq + rr]);
-        m = warp_max(m);
-        float sum = 0.f;
-        for (int s = tid; s < ns; s += 32) {
-            const float w = (m == -INFINITY) ? 0.f : expf(lse_part[(size_t)(p0 + s) * rows_per_seq + rr] - m);
-            if (s < 256) w_s[s] = w;
-            sum += w;
-        }
-        sum = warp_sum(sum);
-        if (tid == 0) {
-            s_inv = sum > 0.f ? 1.f / sum : 0.f;
-            s_lse = sum > 0.f ? m + logf(sum) : -INFINITY;
-        }
-    }
-    __syncthreads();
-    const float inv = s_inv;
-    // float4 columns; eight splits' loads are in flight before any is summed
-    for (int k4 = tid; k4 < d_c / 4; k4 += 128) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s0 = 0; s0 < ns; s0 += 8) {
-            float4 v[8];
-            float wv[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int sp = s0 + u;
-                wv[u] = sp < ns ? w_s[sp] : 0.f;
-                v[u] = wv[u] != 0.f
-                           ? reinterpret_cast<const float4*>(o_part + ((size_t)(p0 + sp) * rows_per_seq + rr) * d_c)[k4]
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int task = blockIdx.x; task < tasks; task += gridDim.x) {
+        const int b = split_list[task / rows_per_seq], rr = task % rows_per_seq;
+        const int row = b * rows_per_seq + rr;      // (b, i, h)
+        const int ns = seq_nsplit[b];
+        const int p0 = seq_part0[b];
+        __syncthreads();                            // w_s / s_inv of the previous task are read
+        if (tid < 32) {
+            float m = -INFINITY;
+            for (int s = tid; s < ns; s += 32) m = fmaxf(m, lse_part[(size_t)(p0 + s) * rows_per_seq + rr]);
+            m = warp_max(m);
+            float sum = 0.f;
+            for (int s = tid; s < ns; s += 32) {
+                const float w = (m == -INFINITY) ? 0.f : expf(lse_part[(size_t)(p0 + s) * rows_per_seq + rr] - m);
+                if (s < 256) w_s[s] = w;
+                sum += w;
             }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                acc.x = fmaf(wv[u], v[u].x, acc.x);
-                acc.y = fmaf(wv[u], v[u].y, acc.y);
-                acc.z = fmaf(wv[u], v[u].z, acc.z);
-                acc.w = fmaf(wv[u], v[u].w, acc.w);
+            sum = warp_sum(sum);
+            if (tid == 0) {
+                s_inv = sum > 0.f ? 1.f / sum : 0.f;
+                s_lse = sum > 0.f ? m + logf(sum) : -INFINITY;
             }
         }
-        acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-        if (o_dtype == QKMLA_F32) {
-            reinterpret_cast<float4*>((float*)o + (size_t)row * d_c)[k4] = acc;
-        } else {
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-            uint2 pk;
-            pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-            pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-            reinterpret_cast<uint2*>((__nv_bfloat16*)o + (size_t)row * d_c)[k4] = pk;
+        __syncthreads();
+        const float inv = s_inv;
+        // float4 columns; eight splits' loads are in flight before any is summed
+        for (int k4 = tid; k4 < d_c / 4; k4 += 128) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s0 = 0; s0 < ns; s0 += 8) {
+                float4 v[8];
+                float wv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int sp = s0 + u;
+                    wv[u] = sp < ns ? w_s[sp] : 0.f;
+                    v[u] = wv[u] != 0.f
+                               ? reinterpret_cast<const float4*>(o_part + ((size_t)(p0 + sp) * rows_per_seq + rr) * d_c)[k4]
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    acc.x = fmaf(wv[u], v[u].x, acc.x);
+                    acc.y = fmaf(wv[u], v[u].y, acc.y);
+                    acc.z = fmaf(wv[u], v[u].z, acc.z);
+                    acc.w = fmaf(wv[u], v[u].w, acc.w);
+                }
+            }
+            acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+            if (o_dtype == QKMLA_F32) {
+                reinterpret_cast<float4*>((float*)o + (size_t)row * d_c)[k4] = acc;
+            } else {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+                uint2 pk;
+                pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+                pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                reinterpret_cast<uint2*>((__nv_bfloat16*)o + (size_t)row * d_c)[k4] = pk;
+            }
         }
+        if (tid == 0 && lse) lse[row] = s_lse;
     }
-    if (tid == 0 && lse) lse[row] = s_lse;
 }
 
 // ---------------------------------------------------------------------------
@@ -772,7 +784,7 @@ size_t tc_workspace(const qkmla_decode_args* a, int sms, int* max_items_out) {
     if (max_items_out) *max_items_out = max_items;
     size_t off = 0;
     off += (size_t)max_items * sizeof(WorkItem);
-    off += 16 + 2 * (size_t)a->B * sizeof(int);
+    off += 16 + 3 * (size_t)a->B * sizeof(int);
     off = (off + 255) & ~(size_t)255;
     off += (size_t)max_items * a->s_q * a->H * a->d_c * sizeof(float);
     off += (size_t)max_items * a->s_q * a->H * sizeof(float);
@@ -791,7 +803,8 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     int* n_items = (int*)(ws + off);
     int* seq_nsplit = n_items + 4;
     int* seq_part0 = seq_nsplit + a->B;
-    off += 16 + 2 * (size_t)a->B * sizeof(int);
+    int* split_list = seq_part0 + a->B;
+    off += 16 + 3 * (size_t)a->B * sizeof(int);
     off = (off + 255) & ~(size_t)255;
     float* o_part = (float*)(ws + off);
     float* lse_part = o_part + (size_t)max_items * a->s_q * a->H * a->d_c;
@@ -801,7 +814,7 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     const int tile = pair_shape(a) ? 64 : a->d_c == 256 ? tile_of<256>() : tile_of<512>();
     const int box = tile;
     if (launch_pdl(sched_kernel, dim3(1), dim3(1024), 0, s, a->seq_lens, a->B, a->s_q, max_len, n_rb, sms,
-                   /*min_tokens=*/512, tile, a->num_splits, items, n_items, seq_nsplit, seq_part0, status) !=
+                   /*min_tokens=*/512, tile, a->num_splits, items, n_items, seq_nsplit, seq_part0, split_list, status) !=
         cudaSuccess)
         return QKMLA_ERR_CUDA;
 
@@ -852,9 +865,10 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
                    : launch_kernel<256, 32, false, 4>(lat, rope, qmap, tp, n_rb, max_items, s);
     }
     if (rc != QKMLA_OK) return rc;
-    return launch_pdl(combine_var_kernel, dim3(a->B * a->s_q * a->H), dim3(128), 0, s, (const float*)o_part,
-                      (const float*)lse_part, (const int*)seq_nsplit, (const int*)seq_part0, a->s_q * a->H, a->d_c,
-                      a->o, a->o_dtype, a->lse) == cudaSuccess
+    const int combine_ctas = std::min(a->B * a->s_q * a->H, 2 * sms);
+    return launch_pdl(combine_var_kernel, dim3(combine_ctas), dim3(128), 0, s, (const float*)o_part,
+                      (const float*)lse_part, (const int*)seq_nsplit, (const int*)seq_part0, (const int*)split_list,
+                      (const int*)(n_items + 1), a->s_q * a->H, a->d_c, a->o, a->o_dtype, a->lse) == cudaSuccess
                ? QKMLA_OK
                : QKMLA_ERR_CUDA;
 }

@@ -58,6 +58,19 @@ def check_close(got, ref, kind, what="", edge=False):
     return float(d.max()), float(rel_l2)
 
 
+def assert_status_ok(Q):
+    """The library's device status word is clear; on a failed stream sync, name the CUDA error."""
+    st = Q.get_device_status()
+    if st == Q.ERR_CUDA:
+        try:
+            torch.cuda.synchronize()
+            msg = "stream sync failed, context still usable"
+        except Exception as e:                      # the sticky error of the context
+            msg = f"{type(e).__name__}: {e}"
+        raise AssertionError(f"device status QKMLA_ERR_CUDA ({msg})")
+    assert st == 0, st
+
+
 def _np(t):
     return t.detach().float().cpu().numpy()
 
@@ -123,7 +136,7 @@ def test_append_matches_oracle_bit_exact_layout(Q, cache, plain, widx):
     ak0 = ak.clone()
     Q.append(torch.from_numpy(c).to(d), torch.from_numpy(r).to(d), torch.from_numpy(wk).to(d),
              torch.from_numpy(grk).to(d), torch.from_numpy(slots).to(d), kv, ak, w.eps, plain=plain)
-    assert Q.get_device_status() == 0
+    assert_status_ok(Q)
     ch, rh, a = O.append_tokens(c, r, wk, grk, w.eps, cache, plain=plain)
     ok = slots >= 0
     kvh = kv.cpu()
@@ -165,7 +178,7 @@ def test_append_bulk_and_plain_kernels_agree(Q, widx):
         ak = torch.zeros((256, w.G), dtype=torch.float32, device="cuda")
         Q.append(cn, torch.from_numpy(r).cuda(), torch.from_numpy(wk).cuda(), torch.from_numpy(grk).cuda(),
                  slots, kv, ak, w.eps)
-        assert Q.get_device_status() == 0
+        assert_status_ok(Q)
         outs.append((kv.view(torch.int16).cpu(), ak.cpu()))
     assert torch.equal(outs[0][0], outs[1][0])
     np.testing.assert_allclose(outs[0][1].numpy(), outs[1][1].numpy(), rtol=2e-6)
@@ -181,7 +194,7 @@ def test_append_out_of_range_slot_is_reported(Q):
     slots = torch.tensor([5, 128], dtype=torch.int64, device="cuda")
     Q.append(c, r, wk, None, slots, kv, ak, w.eps)
     assert Q.get_device_status() == Q.ERR_DEVICE_BOUNDS
-    assert Q.get_device_status() == 0            # cleared by the read
+    assert_status_ok(Q)            # cleared by the read
     assert torch.count_nonzero(kv[5]) > 0
 
 
@@ -219,7 +232,7 @@ def test_decode_end_to_end_matches_oracle(Q, name, plain):
         w = w.with_(outlier_frac=0.0)
     st = DeviceState(w, plain=plain)
     st.step()
-    assert Q.get_device_status() == 0
+    assert_status_ok(Q)
     o_ref, lse_ref = OR.reference(w, plain=plain)
     edge = name in EDGE
     check_close(_np(st.o), o_ref, w.cache_dtype, f"{name} o", edge)
@@ -238,7 +251,7 @@ def test_tensor_core_kernel_is_selected_and_agrees_with_simt(Q, name):
     st.decode(force_simt=True)
     o_s, l_s = _np(st.o).copy(), _np(st.lse).copy()
     st.decode()
-    assert Q.get_device_status() == 0
+    assert_status_ok(Q)
     check_close(_np(st.o), o_s, "bf16", f"{name} tc-vs-simt o")
     check_close(_np(st.lse), l_s, "bf16", f"{name} tc-vs-simt lse")
 
@@ -256,7 +269,7 @@ def test_plain_with_outliers_rescales_agree_across_kernels(Q, name):
     st.append_step()
     for _ in range(3):                          # repeated launches on the same state
         st.decode()
-    assert Q.get_device_status() == 0
+    assert_status_ok(Q)
     o_tc, l_tc = _np(st.o).copy(), _np(st.lse).copy()
     st.decode(force_simt=True)
     o_s, l_s = _np(st.o), _np(st.lse)
@@ -276,7 +289,7 @@ def test_decode_split_counts_agree(Q, splits, simt):
     st.decode(num_splits=0, force_simt=simt)
     o_auto, l_auto = _np(st.o).copy(), _np(st.lse).copy()
     st.decode(num_splits=splits, force_simt=simt)
-    assert Q.get_device_status() == 0
+    assert_status_ok(Q)
     o_ref, lse_ref = OR.reference(w)
     check_close(_np(st.o), o_ref, "bf16", f"splits={splits} o", edge=True)
     check_close(_np(st.lse), lse_ref, "bf16", f"splits={splits} lse", edge=True)
@@ -291,7 +304,7 @@ def test_decode_bad_page_id_is_reported_not_trapped(Q):
     w = _workload("dsv3_ragged")
     st = DeviceState(w)
     st.step()
-    assert Q.get_device_status() == 0
+    assert_status_ok(Q)
     bad = st.page_table.clone()
     bad[5, 3] = 10 ** 6                     # outside [0, num_pages)
     st.page_table = bad
@@ -336,7 +349,7 @@ def test_full_size_sampled_rows(Q, widx, picks, heads):
     w = W.WORKLOADS[widx]
     st = DeviceState(w)
     st.step()
-    assert Q.get_device_status() == 0
+    assert_status_ok(Q)
     if picks == "spread":
         order = np.argsort(W.seq_lens(w))
         picks = (int(order[0]), int(order[len(order) // 2]), int(order[-1]))
