@@ -180,11 +180,6 @@ __device__ __forceinline__ void tma_prefetch_l2(const void* tmap, int x, int y) 
                  ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y)
                  : "memory");
 }
-// Pull `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
-                 : "memory");
-}
 // Cluster-wide barrier (all threads of every CTA of the cluster).  The
 // non-aligned form: callers may arrive from diverged code paths.
 __device__ __forceinline__ void cluster_sync() {

@@ -52,7 +52,6 @@ constexpr int kHalfLat = kDC / 2;  // latent columns per CTA
 constexpr int kHalfRope = kDR / 2; // RoPE columns per CTA
 constexpr int kThreadsP = 320;    // 2 + 4 + 4 warps
 constexpr int kNst = 3;            // TMA stages
-constexpr int kPf = 6;             // L2 prefetch distance in tiles (> kNst, < 32)
 
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr int kQLat = 4 * kR * 128;                    // Q~ half: 4 blocks of 128 rows x 128 B
@@ -197,30 +196,13 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             return (int)(page * p.page_size + (t0 % p.page_size));
         };
         const uint32_t tx = (uint32_t)(kSLat + kSRope) + (PLAIN ? 0u : (uint32_t)(kT * p.G * 4));
-        // L2 prefetch of this CTA's half of a tile (no shared memory, nothing to wait for):
-        // the HBM latency is paid kPf tiles ahead, the stage ring only waits for L2
-        auto prefetch_tile = [&](int slot) {
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) tma_prefetch_l2(&tm_lat, rank * kHalfLat + blk * 64, slot);
-            tma_prefetch_l2(&tm_rope, kDC + rank * kHalfRope, slot);
-            if (!PLAIN) bulk_prefetch_l2(p.ak + (int64_t)slot * p.G, (uint32_t)(kT * p.G * 4));
-        };
         int slot_batch = slot_of_tile(lane);
-        for (int jp = kNst; jp < kPf; ++jp) {            // the tiles the first loads do not cover
-            const int sl = __shfl_sync(0xffffffffu, slot_batch, jp);
-            if (lane == 0 && jp < n_t) prefetch_tile(sl);
-        }
-        int pf_batch = slot_batch;                       // slots of tiles (jp & ~31) + lane
         for (int j = 0; j < n_t; ++j) {
             if ((j & 31) == 0 && j > 0) slot_batch = slot_of_tile(j + lane);
-            const int jp = j + kPf;
-            if ((jp & 31) == 0) pf_batch = slot_of_tile(jp + lane);
             const int slot0 = __shfl_sync(0xffffffffu, slot_batch, j & 31);
-            const int slot_pf = __shfl_sync(0xffffffffu, pf_batch, jp & 31);
             int go = 1;
             if (lane == 0) {
                 const int s = j % kNst;
-                if (jp < n_t && !*(volatile int*)abort_flag) prefetch_tile(slot_pf);
                 if (j >= kNst && !wait_bounded(&empty[s], ((j / kNst) - 1) & 1, p.status)) {
                     *abort_flag = 1;
                     go = 0;

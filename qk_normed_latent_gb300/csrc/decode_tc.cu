@@ -43,7 +43,6 @@ using namespace dec;
 
 constexpr int kRowsMMA = 64;       // M of the logit MMA
 constexpr int kThreads = 192;
-constexpr int kPfAhead = 4;        // L2 prefetch distance in tiles (NST + kPfAhead <= 32)
 
 // Tokens per tile: 64 for d_c = 256, 32 for d_c = 512.  The logit MMA costs the
 // same issue time for any N up to 128, so wider tiles cut its cost per token; the
@@ -181,17 +180,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             tma_load_2d(stg + LY::kSLat, &tm_rope, DC, (int)slot0, &full[s]);
         if (!PLAIN) bulk_load(stg + LY::kSLat + LY::kSRope, p.ak + slot0 * p.G, ak_bytes, &full[s]);
     };
-    // L2 prefetch of a tile kPfAhead loads ahead (no shared memory, nothing to wait
-    // for): the stage ring then waits for L2, not for HBM
-    auto prefetch_tile = [&](int64_t slot0) {            // lane 0 of warp 0
-#pragma unroll
-        for (int blk = 0; blk < LY::kLatBlocks; ++blk) tma_prefetch_l2(&tm_lat, blk * 64, (int)slot0);
-        if (DR == 64)
-            tma_prefetch_l2(&tm_lat, DC, (int)slot0);
-        else
-            tma_prefetch_l2(&tm_rope, DC, (int)slot0);
-        if (!PLAIN) bulk_prefetch_l2(p.ak + slot0 * p.G, ak_bytes);
-    };
     int64_t slot_batch = 0;
 
     if (warp == 0) {
@@ -208,10 +196,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
         for (int j = 0; j < NST && j < n_t; ++j) {
             const int64_t slot0 = __shfl_sync(0xffffffffu, slot_batch, j);
             if (lane == 0) issue_tile(j, slot0);
-        }
-        for (int jp = NST; jp < NST + kPfAhead; ++jp) {   // the tiles the loop's prefetches do not cover
-            const int64_t sl = __shfl_sync(0xffffffffu, slot_batch, jp);
-            if (lane == 0 && jp < n_t) prefetch_tile(sl);
         }
     } else if (warp >= 2) {
         // ---- prologue (softmax warps): the normalised RoPE query, alpha^q, and
@@ -261,17 +245,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
 
     if (warp == 0) {
         // ===================== TMA producer (lane 0 issues; lanes hold page slots) =====================
-        int64_t pf_batch = slot_batch;                 // slots of tiles (jp & ~31) + lane
         for (int j = NST; j < n_t; ++j) {
             if ((j & 31) == 0) slot_batch = slot_of_tile(j + lane);
-            const int jp = j + kPfAhead;
-            if ((jp & 31) == 0) pf_batch = slot_of_tile(jp + lane);
             const int64_t slot0 = __shfl_sync(0xffffffffu, slot_batch, j & 31);
-            const int64_t slot_pf = __shfl_sync(0xffffffffu, pf_batch, jp & 31);
             int go = 1;
             if (lane == 0) {
                 const int s = j % NST;
-                if (jp < n_t && !*(volatile int*)abort_flag) prefetch_tile(slot_pf);
                 if (!wait_bounded(&empty[s], ((j / NST) - 1) & 1, p.status)) {
                     *abort_flag = 1;
                     go = 0;
