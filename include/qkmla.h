@@ -195,8 +195,10 @@ const char* qkmla_decode_kernel_name(const qkmla_decode_args* a);
 
 /*
  * qkmla_decode_launch_count -- number of kernels one qkmla_decode call with
- * these arguments launches on the stream (tensor-core path: split scheduler,
- * decode, combine; CUDA-core path: decode, plus combine when it splits).
+ * these arguments launches on the stream (tensor-core path: decode and
+ * combine, plus a split-scheduler kernel ahead of them for batches of more
+ * than 128 sequences -- smaller batches are planned inside the decode and
+ * combine kernels; CUDA-core path: decode, plus combine when it splits).
  * Returns 0 for arguments qkmla_decode would reject.
  */
 int qkmla_decode_launch_count(const qkmla_decode_args* a);

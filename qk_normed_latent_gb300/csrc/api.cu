@@ -162,7 +162,7 @@ const char* qkmla_decode_kernel_name(const qkmla_decode_args* a) {
 int qkmla_decode_launch_count(const qkmla_decode_args* a) {
     DecodePlan plan;
     if (plan_decode(a, &plan) != QKMLA_OK) return 0;
-    if (plan.kernel == 1) return 3;
+    if (plan.kernel == 1) return sched_in_kernel(a) ? 2 : 3;   // [scheduler,] decode, combine
     return plan.parts > 1 ? 2 : 1;
 }
 

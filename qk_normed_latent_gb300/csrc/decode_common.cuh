@@ -22,6 +22,11 @@ struct WorkItem {
     int part;          // -1: the item is the whole sequence, write the final row
 };
 
+// Parameters of the split-KV schedule (see decode_sched.cuh).
+struct SchedArgs {
+    int max_len, n_rb, sms, min_tokens, tile, fixed_splits;
+};
+
 struct TcParams {
     const __nv_bfloat16* qt;   // [B][s_q][H][d_c]
     const float* aq;           // [B][s_q][H]
@@ -35,8 +40,10 @@ struct TcParams {
     int B, s_q, H, G;
     int rows_o;                // query rows per CTA (N of the output MMA)
     float scale, eps;
-    const WorkItem* items;
+    const WorkItem* items;     // scheduler kernel's plan (when sched_inline == 0)
     const int* n_items;
+    SchedArgs sa;
+    int sched_inline;          // 1: every CTA computes the plan from seq_lens itself
     float* o_part;             // [max_items][s_q*H][d_c]
     float* lse_part;           // [max_items][s_q*H]
     void* o;

@@ -39,6 +39,7 @@
 
 #include "common.cuh"
 #include "decode_common.cuh"
+#include "decode_sched.cuh"
 #include "tc_ptx.cuh"
 
 namespace qkmla {
@@ -110,10 +111,18 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_wait();
     pdl_trigger();
-    if ((int)blockIdx.y >= *p.n_items) return;          // uniform over the cluster
+    WorkItem it;
+    if (p.sched_inline) {                                // both CTAs derive the same plan
+        __shared__ SchedSmem S;
+        compute_schedule(p.seq_lens, p.B, p.s_q, p.sa, S, p.status, blockIdx.x == 0 && blockIdx.y == 0);
+        if ((int)blockIdx.y >= S.n_items) return;        // uniform over the cluster
+        it = schedule_item(S, p.B, (int)blockIdx.y);
+    } else {
+        if ((int)blockIdx.y >= *p.n_items) return;       // uniform over the cluster
+        it = p.items[blockIdx.y];
+    }
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
-    const WorkItem it = p.items[blockIdx.y];
     const int qi = blockIdx.x >> 1;                       // query token of this pair
     const int b = it.b;
     const int seq_len = p.seq_lens[b];

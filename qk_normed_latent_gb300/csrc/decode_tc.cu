@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "decode_common.cuh"
+#include "decode_sched.cuh"
 #include "tc_ptx.cuh"
 
 namespace qkmla {
@@ -121,8 +122,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
     const int item_idx = blockIdx.y;
     pdl_wait();
     pdl_trigger();
-    if (item_idx >= *p.n_items) return;
-    const WorkItem it = p.items[item_idx];
+    WorkItem it;
+    if (p.sched_inline) {
+        __shared__ SchedSmem S;
+        compute_schedule(p.seq_lens, p.B, p.s_q, p.sa, S, p.status, item_idx == 0 && blockIdx.x == 0);
+        if (item_idx >= S.n_items) return;
+        it = schedule_item(S, p.B, item_idx);
+    } else {
+        if (item_idx >= *p.n_items) return;
+        it = p.items[item_idx];
+    }
     const int rows_o = p.rows_o;
     const int row0 = blockIdx.x * rows_o;          // row index within the sequence's s_q*H rows
     const int qi = row0 / p.H, h0 = row0 % p.H;
@@ -633,24 +642,31 @@ sched_kernel(const int32_t* __restrict__ seq_lens, int B, int s_q, int max_len, 
 // ---------------------------------------------------------------------------
 // combine for variable split counts
 // ---------------------------------------------------------------------------
-// A fixed grid walks the rows of the sequences the scheduler split (a compact
-// list it wrote): with no split sequence every CTA reads one count and exits.
+// A fixed grid walks the rows of the split sequences: with none, every CTA exits
+// after the dependency wait.  When the decode kernels planned the split
+// themselves, the combine derives the same plan from seq_lens -- which the decode
+// call does not write -- before its dependency wait, while the decode kernel
+// still runs; otherwise it reads the scheduler kernel's compact list.
 __global__ void __launch_bounds__(128)
 combine_var_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                    const int* __restrict__ seq_nsplit, const int* __restrict__ seq_part0,
-                   const int* __restrict__ split_list, const int* __restrict__ n_split, int rows_per_seq, int d_c,
-                   void* __restrict__ o, int o_dtype, float* __restrict__ lse) {
+                   const int* __restrict__ split_list, const int* __restrict__ n_split,
+                   const int32_t* __restrict__ seq_lens, int B, int s_q, SchedArgs sa, int sched_inline,
+                   int rows_per_seq, int d_c, void* __restrict__ o, int o_dtype, float* __restrict__ lse) {
     __shared__ float w_s[256];
     __shared__ float s_inv, s_lse;
+    __shared__ SchedSmem S;
+    if (sched_inline) compute_schedule(seq_lens, B, s_q, sa, S, nullptr, false);
     pdl_wait();
     pdl_trigger();
-    const int tasks = *n_split * rows_per_seq;
+    const int tasks = (sched_inline ? S.n_split : *n_split) * rows_per_seq;
     const int tid = threadIdx.x;
     for (int task = blockIdx.x; task < tasks; task += gridDim.x) {
-        const int b = split_list[task / rows_per_seq], rr = task % rows_per_seq;
+        const int sq = task / rows_per_seq, rr = task % rows_per_seq;
+        const int b = sched_inline ? S.split[sq] : split_list[sq];
         const int row = b * rows_per_seq + rr;      // (b, i, h)
-        const int ns = seq_nsplit[b];
-        const int p0 = seq_part0[b];
+        const int ns = sched_inline ? S.ns[b] : seq_nsplit[b];
+        const int p0 = sched_inline ? S.base[b] : seq_part0[b];
         __syncthreads();                            // w_s / s_inv of the previous task are read
         if (tid < 32) {
             float m = -INFINITY;
@@ -760,6 +776,9 @@ bool pair_shape(const qkmla_decode_args* a) {
     return a->d_c == 512 && a->d_r == 64 && a->H == 128 && a->page_size % 64 == 0;
 }
 
+// Batches whose split plan every decode CTA computes itself (no scheduler launch).
+bool sched_in_kernel(const qkmla_decode_args* a) { return a->B >= 1 && a->B <= dec::kMaxBSched; }
+
 // Shapes the tensor-core kernel is built for (bf16 cache).
 bool tc_supported(const qkmla_decode_args* a) {
     if (a->cache_dtype != QKMLA_BF16) return false;
@@ -813,9 +832,19 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
 
     const int tile = pair_shape(a) ? 64 : a->d_c == 256 ? tile_of<256>() : tile_of<512>();
     const int box = tile;
-    if (launch_pdl(sched_kernel, dim3(1), dim3(1024), 0, s, a->seq_lens, a->B, a->s_q, max_len, n_rb, sms,
-                   /*min_tokens=*/512, tile, a->num_splits, items, n_items, seq_nsplit, seq_part0, split_list, status) !=
-        cudaSuccess)
+    SchedArgs sa;
+    sa.max_len = max_len;
+    sa.n_rb = n_rb;
+    sa.sms = sms;
+    sa.min_tokens = 512;
+    sa.tile = tile;
+    sa.fixed_splits = a->num_splits;
+    // small batches: the decode and combine kernels plan the split themselves
+    const int sched_inline = sched_in_kernel(a) ? 1 : 0;
+    if (!sched_inline &&
+        launch_pdl(sched_kernel, dim3(1), dim3(1024), 0, s, a->seq_lens, a->B, a->s_q, max_len, n_rb, sms,
+                   sa.min_tokens, tile, a->num_splits, items, n_items, seq_nsplit, seq_part0, split_list, status) !=
+            cudaSuccess)
         return QKMLA_ERR_CUDA;
 
     CUtensorMap lat, rope;
@@ -847,6 +876,8 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     tp.eps = a->eps;
     tp.items = items;
     tp.n_items = n_items;
+    tp.sa = sa;
+    tp.sched_inline = sched_inline;
     tp.o_part = o_part;
     tp.lse_part = lse_part;
     tp.o = a->o;
@@ -868,7 +899,8 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     const int combine_ctas = std::min(a->B * a->s_q * a->H, 2 * sms);
     return launch_pdl(combine_var_kernel, dim3(combine_ctas), dim3(128), 0, s, (const float*)o_part,
                       (const float*)lse_part, (const int*)seq_nsplit, (const int*)seq_part0, (const int*)split_list,
-                      (const int*)(n_items + 1), a->s_q * a->H, a->d_c, a->o, a->o_dtype, a->lse) == cudaSuccess
+                      (const int*)(n_items + 1), a->seq_lens, a->B, a->s_q, sa, sched_inline, a->s_q * a->H,
+                      a->d_c, a->o, a->o_dtype, a->lse) == cudaSuccess
                ? QKMLA_OK
                : QKMLA_ERR_CUDA;
 }

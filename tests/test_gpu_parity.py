@@ -211,8 +211,12 @@ CASES = {
     "mixed_sq2_B3": (4, dict(B=3, lens=(512, 4097, 20000))),
     "small_bf16_B3": (1, dict(B=3, lens=(1024, 1500, 8192))),
     "small_ragged": (1, dict(B=6, lens=(1, 63, 64, 65, 129, 3001))),
+    # more than 128 sequences: the split plan comes from the scheduler kernel
+    # instead of being computed inside the decode and combine kernels
+    "small_B160_sched": (1, dict(B=160, lens=tuple(16 + (37 * i) % 600 for i in range(160)))),
+    "dsv3_B136_sched": (2, dict(B=136, lens=tuple(64 + (53 * i) % 500 for i in range(136)))),
 }
-EDGE = {"dsv3_ragged", "mixed_sq2_ragged", "small_ragged"}
+EDGE = {"dsv3_ragged", "mixed_sq2_ragged", "small_ragged", "small_B160_sched", "dsv3_B136_sched"}
 
 
 def _workload(name):
