@@ -647,12 +647,15 @@ sched_kernel(const int32_t* __restrict__ seq_lens, int B, int s_q, int max_len, 
 // themselves, the combine derives the same plan from seq_lens -- which the decode
 // call does not write -- before its dependency wait, while the decode kernel
 // still runs; otherwise it reads the scheduler kernel's compact list.
+template <int VEC>
 __global__ void __launch_bounds__(128)
 combine_var_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                    const int* __restrict__ seq_nsplit, const int* __restrict__ seq_part0,
                    const int* __restrict__ split_list, const int* __restrict__ n_split,
                    const int32_t* __restrict__ seq_lens, int B, int s_q, SchedArgs sa, int sched_inline,
-                   int rows_per_seq, int d_c, void* __restrict__ o, int o_dtype, float* __restrict__ lse) {
+                   int rows_per_seq, void* __restrict__ o, int o_dtype, float* __restrict__ lse) {
+    constexpr int kDc = 128 * VEC;              // thread t owns columns VEC t .. VEC t + VEC-1
+    constexpr int kRegSplits = 16;              // partials held in registers per thread
     __shared__ float w_s[256];
     __shared__ float s_inv, s_lse;
     __shared__ SchedSmem S;
@@ -668,14 +671,31 @@ combine_var_kernel(const float* __restrict__ o_part, const float* __restrict__ l
         const int ns = sched_inline ? S.ns[b] : seq_nsplit[b];
         const int p0 = sched_inline ? S.base[b] : seq_part0[b];
         __syncthreads();                            // w_s / s_inv of the previous task are read
+        // every thread's loads of the first kRegSplits partials go out now, while
+        // warp 0 turns the partial lse values into weights
+        float v[kRegSplits][VEC];
+#pragma unroll
+        for (int u = 0; u < kRegSplits; ++u) {
+            if (u < ns) {
+                const float* src = o_part + ((size_t)(p0 + u) * rows_per_seq + rr) * kDc + VEC * tid;
+                if constexpr (VEC == 4) {
+                    const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+                    v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+                } else {
+                    const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+                    v[u][0] = x.x; v[u][1] = x.y;
+                }
+            }
+        }
         if (tid < 32) {
             float m = -INFINITY;
-            for (int s = tid; s < ns; s += 32) m = fmaxf(m, lse_part[(size_t)(p0 + s) * rows_per_seq + rr]);
+            for (int s = tid; s < ns; s += 32) m = fmaxf(m, __ldcg(lse_part + (size_t)(p0 + s) * rows_per_seq + rr));
             m = warp_max(m);
             float sum = 0.f;
             for (int s = tid; s < ns; s += 32) {
-                const float w = (m == -INFINITY) ? 0.f : expf(lse_part[(size_t)(p0 + s) * rows_per_seq + rr] - m);
-                if (s < 256) w_s[s] = w;
+                const float w =
+                    (m == -INFINITY) ? 0.f : expf(__ldcg(lse_part + (size_t)(p0 + s) * rows_per_seq + rr) - m);
+                w_s[s] = w;                         // ns <= 256
                 sum += w;
             }
             sum = warp_sum(sum);
@@ -686,37 +706,42 @@ combine_var_kernel(const float* __restrict__ o_part, const float* __restrict__ l
         }
         __syncthreads();
         const float inv = s_inv;
-        // float4 columns; eight splits' loads are in flight before any is summed
-        for (int k4 = tid; k4 < d_c / 4; k4 += 128) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s0 = 0; s0 < ns; s0 += 8) {
-                float4 v[8];
-                float wv[8];
+        float acc[VEC];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int sp = s0 + u;
-                    wv[u] = sp < ns ? w_s[sp] : 0.f;
-                    v[u] = wv[u] != 0.f
-                               ? reinterpret_cast<const float4*>(o_part + ((size_t)(p0 + sp) * rows_per_seq + rr) * d_c)[k4]
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+        for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+        // a split with no tokens has weight 0 and contributes nothing
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    acc.x = fmaf(wv[u], v[u].x, acc.x);
-                    acc.y = fmaf(wv[u], v[u].y, acc.y);
-                    acc.z = fmaf(wv[u], v[u].z, acc.z);
-                    acc.w = fmaf(wv[u], v[u].w, acc.w);
-                }
+        for (int u = 0; u < kRegSplits; ++u) {
+            const float w = u < ns ? w_s[u] : 0.f;
+            if (w != 0.f) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
             }
-            acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-            if (o_dtype == QKMLA_F32) {
-                reinterpret_cast<float4*>((float*)o + (size_t)row * d_c)[k4] = acc;
-            } else {
-                const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        }
+        for (int u = kRegSplits; u < ns; ++u) {
+            const float w = w_s[u];
+            if (w == 0.f) continue;
+            const float* src = o_part + ((size_t)(p0 + u) * rows_per_seq + rr) * kDc + VEC * tid;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[e] = fmaf(w, __ldcg(src + e), acc[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] *= inv;
+        if (o_dtype == QKMLA_F32) {
+            float* dst = (float*)o + (size_t)row * kDc + VEC * tid;
+            if constexpr (VEC == 4) *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            else *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
+        } else {
+            __nv_bfloat16* dst = (__nv_bfloat16*)o + (size_t)row * kDc + VEC * tid;
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]);
+            if constexpr (VEC == 4) {
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2], acc[3]);
                 uint2 pk;
                 pk.x = *reinterpret_cast<const uint32_t*>(&lo);
                 pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-                reinterpret_cast<uint2*>((__nv_bfloat16*)o + (size_t)row * d_c)[k4] = pk;
+                *reinterpret_cast<uint2*>(dst) = pk;
+            } else {
+                *reinterpret_cast<__nv_bfloat162*>(dst) = lo;
             }
         }
         if (tid == 0 && lse) lse[row] = s_lse;
@@ -897,10 +922,11 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     }
     if (rc != QKMLA_OK) return rc;
     const int combine_ctas = std::min(a->B * a->s_q * a->H, 2 * sms);
-    return launch_pdl(combine_var_kernel, dim3(combine_ctas), dim3(128), 0, s, (const float*)o_part,
-                      (const float*)lse_part, (const int*)seq_nsplit, (const int*)seq_part0, (const int*)split_list,
-                      (const int*)(n_items + 1), a->seq_lens, a->B, a->s_q, sa, sched_inline, a->s_q * a->H,
-                      a->d_c, a->o, a->o_dtype, a->lse) == cudaSuccess
+    auto ck = a->d_c == 512 ? combine_var_kernel<4> : combine_var_kernel<2>;   // d_c = 128 x VEC
+    return launch_pdl(ck, dim3(combine_ctas), dim3(128), 0, s, (const float*)o_part, (const float*)lse_part,
+                      (const int*)seq_nsplit, (const int*)seq_part0, (const int*)split_list,
+                      (const int*)(n_items + 1), a->seq_lens, a->B, a->s_q, sa, sched_inline, a->s_q * a->H, a->o,
+                      a->o_dtype, a->lse) == cudaSuccess
                ? QKMLA_OK
                : QKMLA_ERR_CUDA;
 }
