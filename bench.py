@@ -274,22 +274,41 @@ def main():
     kernel = Q.decode_kernel_name(st.args)
     launches_per_step = 1 + (1 if st.c_new is not None else 0) + Q.decode_launch_count(st.args)
 
-    def timed_steps(state, K):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-               torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        for k in range(K):
-            flush.fill_(k & 0xFF)                       # evict the cache from L2 between steps
-            e0, e1, e2 = ev[k]
-            e0.record(stream)
-            state.absorb()
-            state.append_step()
-            e1.record(stream)
-            Q.decode_raw(state.args)
-            e2.record(stream)
+    def capture(calls):
+        """A CUDA graph of `calls` (library calls on one state).  Kernel arguments and
+        tensor maps are fixed at capture; sequence lengths and the split plan are
+        read on the device at every replay."""
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            calls()
+        torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
-        step_ms = [a.elapsed_time(c) for a, _, c in ev]
-        dec_ms = [b.elapsed_time(c) for _, b, c in ev]
-        return step_ms, dec_ms
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            calls()
+        torch.cuda.synchronize()
+        return g
+
+    def graphs_of(state):
+        step_g = capture(lambda: (state.absorb(), state.append_step(), Q.decode_raw(state.args)))
+        dec_g = capture(lambda: Q.decode_raw(state.args))
+        return step_g, dec_g
+
+    def timed(graph, K):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for k in range(K):
+            flush.fill_(k & 0xFF)                       # evict the cache from L2 between replays
+            ev[k][0].record(stream)
+            graph.replay()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    step_graph, dec_graph = graphs_of(st)
+    for _ in range(max(3, args.warmup)):
+        step_graph.replay()
+    torch.cuda.synchronize()
 
     clk = ClockSampler(local)
     if world > 1:
@@ -297,10 +316,12 @@ def main():
     torch.cuda.synchronize()
     clk.start()
     time.sleep(0.3)
-    step_ms, dec_ms = timed_steps(st, args.steps)
+    step_ms = timed(step_graph, args.steps)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
+    # the decode call alone (scheduler if any, decode kernel, combine): the roofline's interval
+    dec_ms = timed(dec_graph, args.steps)
     clocks = clk.stop()
     total_ms = max_over_ranks(sum(step_ms), world, device="cuda")
     if Q.get_device_status() != 0:
@@ -334,12 +355,14 @@ def main():
         for _ in range(3):
             sp.step()
         torch.cuda.synchronize()
-        p_step, p_dec = timed_steps(sp, min(args.steps, 100))
-        q_step, q_dec = timed_steps(st, min(args.steps, 100))
+        sp_step_g, sp_dec_g = graphs_of(sp)
+        kp = min(args.steps, 100)
+        p_step, p_dec = timed(sp_step_g, kp), timed(sp_dec_g, kp)
+        q_step, q_dec = timed(step_graph, kp), timed(dec_graph, kp)
         plain = {"decode_ms": statistics.median(p_dec), "qknorm_decode_ms": statistics.median(q_dec),
                  "overhead_pct": 100.0 * (statistics.median(q_dec) / statistics.median(p_dec) - 1.0),
                  "step_overhead_pct": 100.0 * (statistics.median(q_step) / statistics.median(p_step) - 1.0)}
-        del sp
+        del sp_step_g, sp_dec_g, sp
 
     # end to end through the public API with host buffers: H2D of the step's inputs,
     # the three calls, D2H of o and lse, all inside the timed region
@@ -385,7 +408,10 @@ def main():
                        "d_h": w.d_h, "d_r": w.d_r, "cache": w.cache_dtype,
                        "context_tokens": int(lens.sum()), "n_append_per_seq": w.n_append,
                        "page_size": w.page_size, "parallelism": f"dp{world} (replicas, no collective)",
-                       "l2": "flushed before every step (256 MiB fill outside the timed intervals)"},
+                       "l2": "flushed before every step (256 MiB fill outside the timed intervals)",
+                       "launch": "each step replays a CUDA graph of absorb, append and the decode call; "
+                                 "decode_ms and the roofline replay a graph of the decode call alone; "
+                                 "e2e drives the Python API call by call"},
             "decode_ms": dec_avg,
             "kv_gbs": bytes_alg / (dec_avg * 1e-3) / 1e9,
             "roofline": roof,

@@ -8,17 +8,18 @@
 //
 // Per KV group the key statistic needs k_{t,g} = c^_t W^K_g, a small GEMM
 // [N, d_c] x [d_c, d_h] in fp32; the key itself is reduced to its sum of
-// squares in registers and never leaves the CTA.  The grid is (token tiles) x G;
-// the g = 0 CTAs also store the cast latent and the normalised RoPE key.
+// squares and never leaves the cluster.
 //
 // A decode step appends a handful of tokens, so the kernel's time is the
-// latency of streaming W^K_g (d_c x d_h fp32) through each CTA.  The main
-// kernel therefore moves its operands with bulk copies: the token tile in one
-// copy per token and W^K_g through a ring of kNST stages that are all in
-// flight at once.  Shapes or pointers the bulk copies cannot take (rows that
-// are not multiples of 16 bytes, misaligned bases) go to a plain-load kernel
-// that forms every key element with the same fmaf chain over ascending k (its
-// sum of squares is reduced across lanes in another order).
+// latency of bringing W^K_g (d_c x d_h fp32) on chip.  The main kernel splits
+// the d_c rows of W^K_g -- contiguous in memory -- over a cluster of S CTAs:
+// each CTA brings its token slice and its W slice with bulk copies, forms the
+// partial keys of its 16 tokens over its 64 rows, and CTA 0 of the cluster adds
+// the S partial keys (read from the others' shared memory, in rank order)
+// before squaring.  The g = 0 cluster also stores the cast latent (each CTA its
+// slice) and the normalised RoPE key.  Shapes or pointers the bulk copies cannot
+// take (d_c not a multiple of 64, misaligned bases) go to a plain-load kernel that
+// forms every key element with one fmaf chain over ascending k.
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -31,21 +32,28 @@ constexpr int kKC = 64;        // d_c chunk staged per step (plain-load kernel)
 constexpr int kThreads = 256;
 constexpr int kMaxJ = 8;       // d_h <= 256
 
-// Bulk-copy kernel: a CTA owns FT tokens of one group.  W^K_g streams through a
-// ring of kNST stages of kRows rows; warp w multiplies rows 4w .. 4w+3 of every
-// stage into partial keys for all FT tokens x 32 NJ columns (lane + 32 j), so one
-// float4 of the token tile feeds 4 NJ FMAs.  The eight warps' partial keys are
-// summed in warp order through the (by then idle) ring memory.
-constexpr int kNST = 4;
-constexpr int kRows = 32;      // W^K_g rows per stage, 4 per warp
-static_assert(kRows == 4 * (kThreads / 32), "four rows per warp and stage");
+// Cluster-split kernel: cluster (tile, g) of S CTAs owns kFT tokens of group g;
+// CTA r holds rows [r KS, r KS + KS) of W^K_g (KS = d_c / S = 64) and the same
+// columns of the token tile.
+constexpr int kFT = 16;        // tokens per cluster
+constexpr int kKS = 64;        // d_c rows per CTA
+__host__ __device__ inline int split_smem_bytes(int d_h) {
+    return kFT * kKS * 4 + kKS * d_h * 4 + kFT * d_h * 4 + 16;
+}
 
-__host__ __device__ constexpr int bulk_ft(int nj) { return nj <= 4 ? 16 : 8; }
-inline int bulk_nj(int d_h) { return d_h <= 64 ? 2 : d_h <= 128 ? 4 : 8; }
-inline int bulk_cs_bytes(int ft, int d_c) { return (ft * d_c * 4 + 127) & ~127; }
-__host__ __device__ inline int bulk_ring_bytes(int d_h) { return kNST * kRows * d_h * 4; }
-inline int bulk_smem_bytes(int ft, int d_c, int d_h) {
-    return bulk_cs_bytes(ft, d_c) + bulk_ring_bytes(d_h) + 8 * (1 + kNST);
+// cluster-wide barrier (every thread of every CTA), DSMEM address of rank r, remote load
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_shared_rank(uint32_t smem_addr, uint32_t r) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_addr), "r"(r));
+    return d;
+}
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 // Latent (pure cast) and RoPE key (normalised on its own) of token n into slot s.
@@ -69,136 +77,125 @@ __device__ __forceinline__ void store_token(const float* lat, const float* __res
     }
 }
 
-template <typename CT, int NJ>
-__global__ void __launch_bounds__(kThreads)
-append_bulk_kernel(const float* __restrict__ c_new, const float* __restrict__ r_new, const float* __restrict__ wk,
-                   const float* __restrict__ grk, const int64_t* __restrict__ slots, int N, int G, int d_c,
-                   int d_h, int d_r, float eps, int plain, CT* __restrict__ kv, float* __restrict__ ak,
-                   int64_t num_slots, int* status) {
+// U = d_h / 16 key columns per thread: thread (t, q) owns token t = tid / 16 and
+// columns q + 16 u.
+template <typename CT, int S, int U>
+__global__ void __cluster_dims__(S, 1, 1) __launch_bounds__(kThreads)
+append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r_new, const float* __restrict__ wk,
+                    const float* __restrict__ grk, const int64_t* __restrict__ slots, int N, int G, int d_r,
+                    float eps, int plain, CT* __restrict__ kv, float* __restrict__ ak, int64_t num_slots,
+                    int* status) {
     using namespace tc;
-    constexpr int FT = bulk_ft(NJ);
-    constexpr int TPT = kThreads / FT;           // threads per token in the final reduction
-    static_assert(TPT <= 32 && 32 % TPT == 0, "a token's reducers sit in one warp");
+    constexpr int kDc = S * kKS, kDh = 16 * U;
     extern __shared__ __align__(128) uint8_t sm[];
-    const int cs_bytes = (FT * d_c * 4 + 127) & ~127;
-    float* Cs = reinterpret_cast<float*>(sm);                     // [FT][d_c]
-    float* Ws = reinterpret_cast<float*>(sm + cs_bytes);          // kNST x [kRows][d_h]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + cs_bytes + bulk_ring_bytes(d_h));  // [0] tokens, [1 + s]
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float* Cs = reinterpret_cast<float*>(sm);                              // [kFT][kKS]
+    float* Ws = Cs + kFT * kKS;                                            // [kKS][kDh]
+    float* red = Ws + kKS * kDh;                                           // [kFT][kDh] partial keys
+    uint64_t* bar = reinterpret_cast<uint64_t*>(red + kFT * kDh);
+    const int tid = threadIdx.x;
+    const int rank = (int)(blockIdx.x % S);
     const int g = blockIdx.y;
-    const int n0 = blockIdx.x * FT;
-    const int nvalid = min(FT, N - n0);
-    const int stage_f = kRows * d_h;
-    const uint32_t stage_bytes = (uint32_t)(stage_f * 4);
-    const int n_chunks = d_c / kRows;
-    const float* wg = wk + (int64_t)g * d_c * d_h;
+    const int n0 = (int)(blockIdx.x / S) * kFT;
+    const int nvalid = min(kFT, N - n0);
+    const int k0 = rank * kKS;                                             // first d_c row of this CTA
 
     if (tid == 0) {
-        for (int i = 0; i < 1 + kNST; ++i) mbar_init(&bars[i], 1);
+        mbar_init(bar, 1);
         fence_barrier_init();
     }
     __syncthreads();
     pdl_wait();
     pdl_trigger();
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bars[0], (uint32_t)(nvalid * d_c * 4));
+        mbar_arrive_expect_tx(bar, (uint32_t)((nvalid * kKS + kKS * kDh) * 4));
+        bulk_load(Ws, wk + ((int64_t)g * kDc + k0) * kDh, (uint32_t)(kKS * kDh * 4), bar);
         for (int t = 0; t < nvalid; ++t)
-            bulk_load(Cs + t * d_c, c_new + (int64_t)(n0 + t) * d_c, (uint32_t)(d_c * 4), &bars[0]);
-        for (int c = 0; c < kNST && c < n_chunks; ++c) {
-            mbar_arrive_expect_tx(&bars[1 + c], stage_bytes);
-            bulk_load(Ws + c * stage_f, wg + (int64_t)c * stage_f, stage_bytes, &bars[1 + c]);
-        }
+            bulk_load(Cs + t * kKS, c_new + (int64_t)(n0 + t) * kDc + k0, (uint32_t)(kKS * 4), bar);
     }
-    // the statistic is taken over the STORED latent: round the tile to the cache type in place
-    bool ok = mbar_wait(&bars[0], 0, 1u << 24);
+    // thread (t, q): token t = tid / 16, columns / elements q + 16 v.  What the tail
+    // needs from global memory is loaded now, while the bulk copies are in flight.
+    const int t = tid >> 4, q = tid & 15;
+    const bool tok = t < nvalid;
+    const int64_t slot = tok ? slots[n0 + t] : -1;
+    const bool rope_here = g == 0 && rank == 0 && tok;
+    float rv[4], gv[4];                                                    // d_r <= 64
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const int j = q + 16 * v;
+        rv[v] = (rope_here && j < d_r) ? r_new[(int64_t)(n0 + t) * d_r + j] : 0.f;
+        gv[v] = (rope_here && j < d_r && !plain && grk != nullptr) ? grk[j] : 1.f;
+    }
+    // the statistic is taken over the STORED latent: round the slice to the cache type in place
+    const bool ok = mbar_wait(bar, 0, 1u << 24);
     if (ok) {
-        for (int e = tid; e < FT * d_c; e += kThreads) Cs[e] = (e < nvalid * d_c) ? Elem<CT>::cast(Cs[e]) : 0.f;
+        for (int e = tid; e < kFT * kKS; e += kThreads) Cs[e] = (e < nvalid * kKS) ? Elem<CT>::cast(Cs[e]) : 0.f;
+    } else {
+        report(status, QKMLA_ERR_TIMEOUT);
     }
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) report(status, QKMLA_ERR_TIMEOUT);
-        return;
-    }
-
-    float acc[FT][NJ];
+    const bool all_ok = __syncthreads_and(ok) != 0;
+    // partial keys over this CTA's rows, one fmaf chain per element over ascending k
+    float acc[U];
 #pragma unroll
-    for (int t = 0; t < FT; ++t)
+    for (int u = 0; u < U; ++u) acc[u] = 0.f;
+    if (all_ok) {
+        const float* cr = Cs + t * kKS;
+#pragma unroll 4
+        for (int k = 0; k < kKS; ++k) {
+            const float a = cr[k];
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) acc[t][j] = 0.f;
-    for (int c = 0; c < n_chunks; ++c) {
-        const int s = c % kNST;
-        ok = mbar_wait(&bars[1 + s], (uint32_t)((c / kNST) & 1), 1u << 24);
-        if (ok) {
-            const float* wr = Ws + s * stage_f + 4 * warp * d_h;
-            float bw[4][NJ];
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                for (int j = 0; j < NJ; ++j) {
-                    const int col = lane + 32 * j;
-                    bw[kk][j] = col < d_h ? wr[kk * d_h + col] : 0.f;
-                }
-            const float* ap = Cs + c * kRows + 4 * warp;
-#pragma unroll
-            for (int t = 0; t < FT; ++t) {
-                const float4 a = *reinterpret_cast<const float4*>(ap + t * d_c);
-#pragma unroll
-                for (int j = 0; j < NJ; ++j) {
-                    acc[t][j] = fmaf(a.x, bw[0][j], acc[t][j]);
-                    acc[t][j] = fmaf(a.y, bw[1][j], acc[t][j]);
-                    acc[t][j] = fmaf(a.z, bw[2][j], acc[t][j]);
-                    acc[t][j] = fmaf(a.w, bw[3][j], acc[t][j]);
-                }
-            }
-        }
-        // every thread is done with stage s before it is refilled
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) report(status, QKMLA_ERR_TIMEOUT);
-            return;
-        }
-        if (tid == 0 && c + kNST < n_chunks) {
-            mbar_arrive_expect_tx(&bars[1 + s], stage_bytes);
-            bulk_load(Ws + s * stage_f, wg + (int64_t)(c + kNST) * stage_f, stage_bytes, &bars[1 + s]);
+            for (int u = 0; u < U; ++u) acc[u] = fmaf(a, Ws[k * kDh + q + 16 * u], acc[u]);
         }
     }
-
-    // every stage has been consumed and no copy is in flight: the ring holds the
-    // partial keys red[warp][t][col] (8 FT d_h floats <= the ring)
-    float* red = Ws;
 #pragma unroll
-    for (int t = 0; t < FT; ++t)
+    for (int u = 0; u < U; ++u) red[t * kDh + q + 16 * u] = acc[u];
+    const bool slot_ok = tok && slot >= 0 && slot < num_slots;
+    // g = 0: this CTA's slice of the token's latent (a pure cast)
+    if (g == 0 && all_ok && slot_ok) {
+        CT* dst = kv + slot * (int64_t)(kDc + d_r) + k0;
 #pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-            const int col = lane + 32 * j;
-            if (col < d_h) red[(warp * FT + t) * d_h + col] = acc[t][j];
-        }
-    __syncthreads();
-    // alpha^k_{t,g} = 1 / sqrt(mean_j k_j^2 + eps): TPT threads per token
-    {
-        const int t = tid / TPT, q = tid % TPT;
+        for (int v = 0; v < kKS / 16; ++v) Elem<CT>::store(dst + q + 16 * v, Cs[t * kKS + q + 16 * v]);
+    }
+    cluster_sync_all();                    // every CTA's partial keys are in its shared memory
+    if (rank == 0) {
+        // k = sum over the cluster's CTAs in rank order, then the sum of squares
+        // over this thread's columns and across the 16 threads of the token
         float ss = 0.f;
-        for (int col = q; col < d_h; col += TPT) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t off = smem_u32(red + t * kDh + q + 16 * u);
             float k = 0.f;
 #pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) k += red[(w * FT + t) * d_h + col];
+            for (int r = 0; r < S; ++r) k += ld_shared_cluster_f32(map_shared_rank(off, (uint32_t)r));
             ss = fmaf(k, k, ss);
         }
 #pragma unroll
-        for (int o = TPT / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (q == 0 && t < nvalid) {
-            const int64_t sl = slots[n0 + t];
-            if (sl >= num_slots) {
+        for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (q == 0 && tok && all_ok) {
+            if (slot >= num_slots) {
                 report(status, QKMLA_ERR_DEVICE_BOUNDS);
-            } else if (sl >= 0) {
-                ak[sl * G + g] = plain ? 1.f : 1.f / sqrtf(ss / (float)d_h + eps);
+            } else if (slot >= 0) {
+                ak[slot * G + g] = plain ? 1.f : 1.f / sqrtf(ss / (float)kDh + eps);
+            }
+        }
+        // the RoPE key, normalised on its own: the token's 16 threads hold its d_r values
+        if (g == 0) {
+            float sr = 0.f;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) sr = fmaf(rv[v], rv[v], sr);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, o);
+            const float beta = plain ? 1.f : 1.f / sqrtf(sr / (float)d_r + eps);
+            if (all_ok && slot_ok) {
+                CT* dst = kv + slot * (int64_t)(kDc + d_r) + kDc;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int j = q + 16 * v;
+                    if (j < d_r) Elem<CT>::store(dst + j, plain ? rv[v] : rv[v] * gv[v] * beta);
+                }
             }
         }
     }
-    if (g != 0) return;
-    for (int t = warp; t < nvalid; t += kThreads / 32) {
-        const int64_t sl = slots[n0 + t];
-        if (sl < 0 || sl >= num_slots) continue;
-        store_token<CT>(Cs + t * d_c, r_new, grk, n0 + t, sl, d_c, d_r, eps, plain, kv, lane);
-    }
+    cluster_sync_all();                    // CTA 0 has read every CTA's partial keys
 }
 
 template <typename CT>
@@ -281,22 +278,33 @@ append_plain_kernel(const float* __restrict__ c_new, const float* __restrict__ r
     }
 }
 
+template <typename CT, int S>
+cudaError_t launch_split(int U, const float* c_new, const float* r_new, const float* wk, const float* grk,
+                         const int64_t* slots, int N, int G, int d_r, float eps, bool plain, CT* kv, float* ak,
+                         int64_t num_slots, cudaStream_t s) {
+    auto k = U == 4 ? append_split_kernel<CT, S, 4> : append_split_kernel<CT, S, 8>;
+    const int smem = split_smem_bytes(16 * U);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(((N + kFT - 1) / kFT) * S, G);
+    return launch_pdl(k, grid, dim3(kThreads), smem, s, c_new, r_new, wk, grk, slots, N, G, d_r, eps, (int)plain, kv,
+                      ak, num_slots, device_status_ptr());
+}
+
 template <typename CT>
 int launch_t(const float* c_new, const float* r_new, const float* wk, const float* grk, const int64_t* slots, int N,
              int G, int d_c, int d_h, int d_r, float eps, bool plain, CT* kv, float* ak, int64_t num_slots,
              cudaStream_t s) {
-    const int nj = bulk_nj(d_h), ft = bulk_ft(nj);
-    const int smem_bulk = bulk_smem_bytes(ft, d_c, d_h);
-    const bool bulk = d_c % kRows == 0 && ((uintptr_t)c_new % 16) == 0 && ((uintptr_t)wk % 16) == 0 &&
-                      smem_bulk <= 232448;
-    if (bulk) {
-        auto k = nj == 2 ? append_bulk_kernel<CT, 2> : nj == 4 ? append_bulk_kernel<CT, 4> : append_bulk_kernel<CT, 8>;
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bulk) != cudaSuccess)
-            return QKMLA_ERR_CUDA;
-        dim3 grid((N + ft - 1) / ft, G);
-        if (launch_pdl(k, grid, dim3(kThreads), smem_bulk, s, c_new, r_new, wk, grk, slots, N, G, d_c, d_h, d_r, eps,
-                       (int)plain, kv, ak, num_slots, device_status_ptr()) != cudaSuccess)
-            return QKMLA_ERR_CUDA;
+    const int S = d_c / kKS;
+    const bool split = d_c % kKS == 0 && (S == 2 || S == 4 || S == 8) && (d_h == 64 || d_h == 128) && d_r <= 64 &&
+                       ((uintptr_t)c_new % 16) == 0 && ((uintptr_t)wk % 16) == 0;
+    if (split) {
+        const int U = d_h / 16;
+        const cudaError_t e =
+            S == 2   ? launch_split<CT, 2>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, num_slots, s)
+            : S == 4 ? launch_split<CT, 4>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, num_slots, s)
+                     : launch_split<CT, 8>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, num_slots, s);
+        if (e != cudaSuccess) return QKMLA_ERR_CUDA;
     } else {
         auto k = append_plain_kernel<CT>;
         const size_t smem = (size_t)kKC * d_h * sizeof(float);

@@ -160,11 +160,12 @@ def test_append_matches_oracle_bit_exact_layout(Q, cache, plain, widx):
 
 
 @pytest.mark.parametrize("widx", [1, 2])
-def test_append_bulk_and_plain_kernels_agree(Q, widx):
+def test_append_cluster_and_plain_kernels_agree(Q, widx):
     """A misaligned token buffer sends qkmla_append to its plain-load kernel.  The
-    cache rows are pure casts and must match bit for bit; both kernels form each
-    key element with the same fp32 FMA chain but reduce the sum of squares over
-    the d_h elements in another order, so alpha^k agrees to fp32 rounding."""
+    cache rows are pure casts and must match bit for bit.  The plain kernel forms
+    each key element with one fp32 FMA chain over d_c; the cluster kernel adds
+    per-slice chains (64 rows each) and reduces the sum of squares in another
+    order, so alpha^k agrees to fp32 rounding."""
     w = W.WORKLOADS[widx]
     wk, _, _, _, grk = W.weights(w)
     c, r = W.sequence(W.small(w, 1, (77,)), 0)
