@@ -142,8 +142,8 @@ def traffic_from_profiles(kernel_sig: str):
     return None
 
 
-DECODE_SOURCES = ("common.cuh", "tc_ptx.cuh", "decode_common.cuh", "decode_tc.cu", "decode_pair.cu",
-                  "decode_simt.cu")
+DECODE_SOURCES = ("common.cuh", "tc_ptx.cuh", "decode_common.cuh", "decode_sched.cuh", "decode_tc.cu",
+                  "decode_pair.cu", "decode_simt.cu")
 
 
 def kernel_signature():
