@@ -112,20 +112,22 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     pdl_wait();
     pdl_trigger();
     WorkItem it;
+    int seq_len;
     if (p.sched_inline) {                                // both CTAs derive the same plan
         __shared__ SchedSmem S;
         compute_schedule(p.seq_lens, p.B, p.s_q, p.sa, S, p.status, blockIdx.x == 0 && blockIdx.y == 0);
         if ((int)blockIdx.y >= S.n_items) return;        // uniform over the cluster
         it = schedule_item(S, p.B, (int)blockIdx.y);
+        seq_len = S.len[it.b];                           // the plan's copy
     } else {
         if ((int)blockIdx.y >= *p.n_items) return;       // uniform over the cluster
         it = p.items[blockIdx.y];
+        seq_len = p.seq_lens[it.b];
     }
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
     const int qi = blockIdx.x >> 1;                       // query token of this pair
     const int b = it.b;
-    const int seq_len = p.seq_lens[b];
     const bool bad = seq_len < p.s_q || seq_len > p.max_pages * p.page_size;
     const int L = bad ? 0 : seq_len - p.s_q + qi + 1;
     const int tiles = (L + kT - 1) / kT;

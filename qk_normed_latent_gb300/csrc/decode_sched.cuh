@@ -23,6 +23,7 @@ namespace dec {
 constexpr int kMaxBSched = 128;
 
 struct SchedSmem {
+    int len[kMaxBSched];       // seq_lens[b] as read
     int tb[kMaxBSched];        // tiles of sequence b
     int ns[kMaxBSched];        // items of sequence b
     int base[kMaxBSched];      // first item of sequence b
@@ -41,6 +42,7 @@ __device__ __forceinline__ void compute_schedule(const int32_t* __restrict__ seq
     int tot = 0, mx = 0;
     for (int b = tid; b < B; b += nt) {
         const int L = __ldcg(seq_lens + b);   // through L2: the lengths may change between calls
+        S.len[b] = L;
         int tl = 0;
         if (L < s_q || L > a.max_len) {
             if (report_errors) report(status, QKMLA_ERR_DEVICE_BOUNDS);

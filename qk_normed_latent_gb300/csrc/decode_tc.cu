@@ -123,20 +123,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
     pdl_wait();
     pdl_trigger();
     WorkItem it;
+    int seq_len;
     if (p.sched_inline) {
         __shared__ SchedSmem S;
         compute_schedule(p.seq_lens, p.B, p.s_q, p.sa, S, p.status, item_idx == 0 && blockIdx.x == 0);
         if (item_idx >= S.n_items) return;
         it = schedule_item(S, p.B, item_idx);
+        seq_len = S.len[it.b];                     // the plan's copy: no second trip to memory
     } else {
         if (item_idx >= *p.n_items) return;
         it = p.items[item_idx];
+        seq_len = p.seq_lens[it.b];
     }
     const int rows_o = p.rows_o;
     const int row0 = blockIdx.x * rows_o;          // row index within the sequence's s_q*H rows
     const int qi = row0 / p.H, h0 = row0 % p.H;
     const int b = it.b;
-    const int seq_len = p.seq_lens[b];
     const bool bad = seq_len < p.s_q || seq_len > p.max_pages * p.page_size;
     const int L = bad ? 0 : seq_len - p.s_q + qi + 1;
     const int tiles = (L + KT - 1) / KT;
