@@ -12,7 +12,8 @@
 // lo = bf16(x - hi)) and three MMAs accumulate hi*hi + hi*lo + lo*hi in fp32
 // (the dropped lo*lo term is ~2^-16 relative).
 //
-// A CTA owns a 128-row x 256-latent output tile of one group.  Its raw fp32
+// A CTA owns a 128-row x NB-latent output tile of one group (NB = 256, or 64
+// when the 256-wide grid would leave most SMs idle: small batches).  Its raw fp32
 // operands land in shared memory by bulk copies (one per query row, eight for
 // the W_g slice), all in flight at once; the 512 threads then split them into
 // bf16 hi/lo in place (each thread reads its elements, a barrier, then writes
@@ -27,7 +28,7 @@ namespace {
 using namespace tc;
 
 constexpr int kM = 128;          // rows per CTA (MMA M)
-constexpr int kN = 256;          // latent columns per CTA (MMA N)
+constexpr int kNMax = 256;       // latent columns per CTA (MMA N) for large grids
 constexpr int kThreads = 512;
 
 __device__ __forceinline__ void split_store(uint8_t* hi_base, uint8_t* lo_base, uint32_t off, const float (&x)[8]) {
@@ -49,7 +50,7 @@ __device__ __forceinline__ void split_store(uint8_t* hi_base, uint8_t* lo_base, 
 // K-major, 128-byte swizzle, 64-column blocks) over the same bytes; B region
 // likewise for [kN][DH].  Thread t handles the 8-element groups
 // e = t + i * kThreads (row e / kG8, columns 8 (e % kG8) .. +7).
-template <int DH>
+template <int DH, int kN>
 struct AbsLayout {
     static constexpr int kA = kM * DH * 4;                    // raw A bytes = A_hi + A_lo bytes
     static constexpr int kB = kN * DH * 4;
@@ -64,12 +65,12 @@ struct AbsLayout {
     static constexpr int kBCopies = 8;
 };
 
-template <int DH, typename OutT>
+template <int DH, int kN, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
 absorb_tc_kernel(const float* __restrict__ q, const float* __restrict__ gq, const float* __restrict__ gk,
                  const float* __restrict__ wk, int rows, int H, int G, int d_c, float eps, int plain,
                  OutT* __restrict__ qt, float* __restrict__ aq, int* status) {
-    using LY = AbsLayout<DH>;
+    using LY = AbsLayout<DH, kN>;
     static_assert(LY::kAIter * kThreads == kM * LY::kG8 && LY::kBIter * kThreads == kN * LY::kG8, "tiling");
     static_assert(32 % LY::kG8 == 0, "a row's groups sit in one warp");
     static_assert(LY::kB % (LY::kBCopies * 16) == 0, "bulk copy sizes");
@@ -212,20 +213,21 @@ absorb_tc_kernel(const float* __restrict__ q, const float* __restrict__ gq, cons
     tc_fence_after();
 
     // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (output rows) and
-    //      columns 64 (w / 4) .. +63 (latent coordinates n0 + ...) ----
+    //      columns kN/4 (w / 4) .. (latent coordinates n0 + ...) ----
+    constexpr int kC16 = kN / 64;                  // 16-column chunks per warp
     if (__all_sync(0xffffffffu, ok)) {
         const int ml = 32 * (warp & 3) + lane;
-        const int c_base = 64 * (warp >> 2);
+        const int c_base = (kN / 4) * (warp >> 2);
         const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + c_base;
-        uint32_t v[4][16];
+        uint32_t v[kC16][16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld16(taddr + 16 * c, v[c]);
+        for (int c = 0; c < kC16; ++c) tmem_ld16(taddr + 16 * c, v[c]);
         tmem_wait_ld();
         if (ml < m_valid) {
             const int m = m0 + ml, r = m / hpg, h = g * hpg + m % hpg;
             OutT* dst = qt + ((size_t)r * H + h) * d_c + n0 + c_base;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < kC16; ++c) {
                 if constexpr (sizeof(OutT) == 2) {
                     uint32_t w[8];
 #pragma unroll
@@ -256,12 +258,12 @@ absorb_tc_kernel(const float* __restrict__ q, const float* __restrict__ gq, cons
     }
 }
 
-template <int DH, typename OutT>
-int launch_t(const float* q, const float* gq, const float* gk, const float* wk, int rows, int H, int G, int d_c,
+template <int DH, int kN, typename OutT>
+int launch_n(const float* q, const float* gq, const float* gk, const float* wk, int rows, int H, int G, int d_c,
              float eps, bool plain, void* qt, float* aq, cudaStream_t s) {
-    using LY = AbsLayout<DH>;
+    using LY = AbsLayout<DH, kN>;
     static_assert(LY::kBytes <= 232448, "shared memory budget");
-    auto k = absorb_tc_kernel<DH, OutT>;
+    auto k = absorb_tc_kernel<DH, kN, OutT>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes) != cudaSuccess)
         return QKMLA_ERR_CUDA;
     const int M = rows * (H / G);
@@ -272,13 +274,23 @@ int launch_t(const float* q, const float* gq, const float* gk, const float* wk, 
                : QKMLA_ERR_CUDA;
 }
 
+// 256-latent tiles, or 64-latent ones when the 256-wide grid has fewer than 64 CTAs.
+template <int DH, typename OutT>
+int launch_t(const float* q, const float* gq, const float* gk, const float* wk, int rows, int H, int G, int d_c,
+             float eps, bool plain, void* qt, float* aq, cudaStream_t s) {
+    const int M = rows * (H / G);
+    const int ctas_wide = ((M + kM - 1) / kM) * (d_c / kNMax) * G;
+    return ctas_wide < 64 ? launch_n<DH, 64, OutT>(q, gq, gk, wk, rows, H, G, d_c, eps, plain, qt, aq, s)
+                          : launch_n<DH, kNMax, OutT>(q, gq, gk, wk, rows, H, G, d_c, eps, plain, qt, aq, s);
+}
+
 }  // namespace
 
 // Shapes the tensor-core absorb handles: d_h in {64, 128}, d_c a multiple of
 // 256, 16-byte aligned fp32 inputs.
 bool absorb_tc_supported(const float* q, const float* wk, int d_h, int d_c) {
     if (d_h != 64 && d_h != 128) return false;
-    if (d_c % kN) return false;
+    if (d_c % kNMax) return false;
     if (((uintptr_t)q % 16) || ((uintptr_t)wk % 16)) return false;
     return true;
 }
