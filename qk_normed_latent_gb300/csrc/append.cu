@@ -131,6 +131,7 @@ append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r
         for (int e = tid; e < kFT * kKS; e += kThreads) Cs[e] = (e < nvalid * kKS) ? Elem<CT>::cast(Cs[e]) : 0.f;
     } else {
         report(status, QKMLA_ERR_TIMEOUT);
+        mbar_wait(bar, 0, 1u << 24);       // copies still in flight land before the CTA's memory is released
     }
     const bool all_ok = __syncthreads_and(ok) != 0;
     // partial keys over this CTA's rows, one fmaf chain per element over ascending k

@@ -118,14 +118,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
     return r;
 }
-// 16-byte store into another CTA's shared memory that completes `bytes` on the
-// mbarrier at `remote_bar` (in that CTA) once the data is visible there.
-__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c, float d,
-                                            uint32_t remote_bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
-                 ::"r"(remote_addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
-                 : "memory");
-}
 // Bounded wait with cluster-scope acquire (data written by the other CTA).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
@@ -149,14 +141,6 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t par
         }
     }
 }
-// Arrive (once) on the mbarrier at the same offset in every CTA of `cta_mask`
-// when all MMAs issued so far by this thread have completed.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-        ::"r"(smem_u32(bar)), "h"(cta_mask)
-        : "memory");
-}
 // Bulk copy from this CTA's shared memory into another CTA's (of the cluster),
 // completing `bytes` on the mbarrier `remote_bar` there.
 __device__ __forceinline__ void bulk_copy_to_cta(uint32_t remote_dst, const void* local_src, uint32_t bytes,
@@ -168,10 +152,6 @@ __device__ __forceinline__ void bulk_copy_to_cta(uint32_t remote_dst, const void
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk copy has finished READING its source.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// Arrive once on an mbarrier of another CTA of the cluster (release, cluster scope).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
-}
 // Relaxed remote arrive: only orders this thread's earlier READS of the rows the
 // other CTA will overwrite (their values are already consumed), no release fence.
 // `dep` is a value computed from every read that must complete first; taking it
@@ -180,12 +160,6 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar, 
     asm volatile("{\n\t.reg .f32 d;\n\tmov.f32 d, %1;\n\t"
                  "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n\t}"
                  ::"r"(remote_bar), "f"(dep) : "memory");
-}
-// Pull a 2-D tensor-map box into L2 ahead of its TMA load.
-__device__ __forceinline__ void tma_prefetch_l2(const void* tmap, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y)
-                 : "memory");
 }
 // Cluster-wide barrier (all threads of every CTA of the cluster).  The
 // non-aligned form: callers may arrive from diverged code paths.

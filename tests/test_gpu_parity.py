@@ -220,6 +220,29 @@ CASES = {
 EDGE = {"dsv3_ragged", "mixed_sq2_ragged", "small_ragged", "small_B160_sched", "dsv3_B136_sched"}
 
 
+def make_args_only(Q, w):
+    """qkmla_decode arguments for workload w on empty (uninitialised) buffers: enough
+    for the host-side planning calls, which read shapes and pointers only."""
+    lens = W.seq_lens(w)
+    ps, max_pages, num_slots, table = W.page_layout(w, lens)
+    dt = torch.bfloat16 if w.cache_dtype == "bf16" else torch.float32
+    d = "cuda"
+    keep = dict(
+        qt=torch.empty((w.B, w.s_q, w.H, w.d_c), dtype=dt, device=d),
+        aq=torch.empty((w.B, w.s_q, w.H), dtype=torch.float32, device=d),
+        qr=torch.empty((w.B, w.s_q, w.H, w.d_r), dtype=torch.float32, device=d),
+        kv=torch.empty((num_slots, w.d_c + w.d_r), dtype=dt, device=d),
+        ak=torch.empty((num_slots, w.G), dtype=torch.float32, device=d),
+        sl=torch.from_numpy(lens.astype(np.int32)).to(d),
+        pt=torch.from_numpy(table).to(d),
+        o=torch.empty((w.B, w.s_q, w.H, w.d_c), dtype=torch.float32, device=d),
+        lse=torch.empty((w.B, w.s_q, w.H), dtype=torch.float32, device=d))
+    a = Q.make_decode_args(keep["qt"], keep["aq"], keep["qr"], None, keep["kv"], keep["ak"], keep["sl"],
+                           keep["pt"], ps, max_pages, w.G, w.scale, w.eps, keep["o"], keep["lse"])
+    a._keep = keep                    # the buffers live as long as the arguments
+    return a
+
+
 def _workload(name):
     widx, red = CASES[name]
     w = W.WORKLOADS[widx]
@@ -259,6 +282,16 @@ def test_tensor_core_kernel_is_selected_and_agrees_with_simt(Q, name):
     assert_status_ok(Q)
     check_close(_np(st.o), o_s, "bf16", f"{name} tc-vs-simt o")
     check_close(_np(st.lse), l_s, "bf16", f"{name} tc-vs-simt lse")
+
+
+@pytest.mark.parametrize("name,launches", [("small_bf16_B3", 2), ("dsv3_B4_T4096", 2), ("small_B160_sched", 3)])
+def test_decode_launch_count(Q, name, launches):
+    """Up to 128 sequences the decode and combine kernels plan the split themselves
+    (two launches); larger batches add the scheduler kernel."""
+    w = _workload(name)
+    a = make_args_only(Q, w)
+    assert Q.decode_kernel_name(a) == "tcgen05"
+    assert Q.decode_launch_count(a) == launches
 
 
 @pytest.mark.parametrize("name", ["dsv3_B4_T4096", "mixed_sq2_B3", "small_bf16_B3"])
