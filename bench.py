@@ -146,14 +146,23 @@ DECODE_SOURCES = ("common.cuh", "tc_ptx.cuh", "decode_common.cuh", "decode_sched
                   "decode_pair.cu", "decode_simt.cu")
 
 
-def kernel_signature():
-    """Hash of the sources the decode kernels are compiled from: a traffic
-    figure recorded under another hash belongs to a kernel that has changed."""
+def code_of(text: str) -> str:
+    """C++/CUDA source without comments and with whitespace collapsed."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_signature(csrc=None):
+    """Hash of the code (comments and layout aside) the decode kernels are
+    compiled from: a traffic figure recorded under another hash belongs to a
+    kernel that has changed."""
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "qk_normed_latent_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "qk_normed_latent_gb300", "csrc")
     for f in DECODE_SOURCES:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        h.update(code_of(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

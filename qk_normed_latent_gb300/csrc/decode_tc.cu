@@ -7,13 +7,14 @@
 // Significance section's note that speed depends on fusing the scalar factors
 // into the attention path.  Values are the latents (latent decode path).
 //
-// Work decomposition.  A CTA owns 64 query rows (heads of one query token) of
-// one sequence and a contiguous range of 32-token tiles.  Per tile:
-//   S_c = Q~ C^T   (M=64 rows, N=32 tokens, K=d_c)   tcgen05, fp32 in TMEM
-//   S_r = Q^r K^rT (M=64,      N=32,        K=d_r)   tcgen05, fp32 in TMEM
+// Work decomposition.  A CTA owns up to 64 query rows (heads of one query
+// token) of one sequence and a contiguous range of tiles (64 tokens for
+// d_c = 256, 32 for d_c = 512).  Per tile:
+//   S_c = Q~ C^T   (M=64 rows, N=tile tokens, K=d_c)   tcgen05, fp32 in TMEM
+//   S_r = Q^r K^rT (M=64,      N=tile tokens, K=d_r)   tcgen05, fp32 in TMEM
 //   l   = scale*(alpha^q_row * alpha^k_{t,g(row)} * S_c + S_r)      (fused, fp32)
 //   P   = exp2(l*log2e - m_row), stored bf16 into the tile's RoPE slot
-//   O^T += C^T P^T (M=128 latent coords per chunk, N=64 rows, K=32 tokens)
+//   O^T += C^T P^T (M=128 latent coords per chunk, N=rows, K=tile tokens)
 // O is kept transposed in TMEM (latent coordinate = lane, row = column): 64 rows
 // x 512 latents take 256 of the 512 TMEM columns, leaving room for two S
 // buffers.  The running max only moves when a tile's max exceeds it by more
@@ -24,8 +25,10 @@
 // allocation), warp 1 issues MMAs, warps 2-5 do the softmax, the rescale and
 // the epilogue.  Every wait is bounded; on expiry QKMLA_ERR_TIMEOUT is recorded.
 //
-// A device-side scheduler turns seq_lens into work items (sequence, tile
-// range); long sequences are split and merged afterwards by a combine kernel.
+// The split plan (work items: sequence, tile range) comes from seq_lens on the
+// device -- computed by every CTA itself for up to 128 sequences, by a
+// scheduler kernel beyond; long sequences are split and merged afterwards by a
+// combine kernel.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
