@@ -399,3 +399,34 @@ def test_full_size_sampled_rows(Q, widx, picks, heads):
     check_close(lse[:, :, hsel], lse_ref[:, :, hsel], w.cache_dtype, f"w{widx} lse")
     # every output row is finite and lse is bounded by the normalised-logit bound
     assert np.all(np.isfinite(_np(st.o))) and np.all(np.isfinite(_np(st.lse)))
+
+
+@pytest.mark.parametrize("widx", [1, 2])
+def test_graph_replay_matches_direct_calls(Q, widx):
+    """bench.py replays a CUDA graph of one step (absorb, append, decode call).  The
+    graph holds the same kernels with the same arguments and the split plan is made
+    on the device, so a replay must reproduce the direct calls bit for bit."""
+    from qk_normed_latent_gb300.pipeline import DeviceState
+    w = W.WORKLOADS[widx]
+    st = DeviceState(w)
+    st.step()
+    assert_status_ok(Q)
+    o1, l1 = st.o.clone(), st.lse.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        st.step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    st.o.zero_()
+    st.lse.zero_()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        st.absorb()
+        st.append_step()
+        Q.decode_raw(st.args)
+    g.replay()
+    torch.cuda.synchronize()
+    assert_status_ok(Q)
+    assert torch.equal(st.o, o1) and torch.equal(st.lse, l1)
