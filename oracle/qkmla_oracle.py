@@ -28,7 +28,7 @@ full key caching", arXiv 2606.16310):
          to explicit post-projection QK RMSNorm in exact arithmetic and keeps
          MLA's latent decode path.
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings where the pages are silent:
   * g(h) = h // (H/G) (contiguous head groups).
   * gamma_q, gamma_k are one [d_h] vector each, shared by all heads/groups.
   * S(z) = sqrt(mean(z^2) + eps) over the d_h entries of one head/group
