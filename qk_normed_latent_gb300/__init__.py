@@ -146,28 +146,51 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def absorb_query(q, gamma_q, gamma_k, w_k, eps: float, q_tilde, alpha_q, plain: bool = False, stream=None):
-    """q [rows, H, d_h] fp32 -> q_tilde [rows, H, d_c] (fp32/bf16), alpha_q [rows, H] fp32."""
+class Prepared:
+    """One library call with its arguments marshalled once: the tensors must stay
+    alive and in place; a call only adds the stream."""
+
+    def __init__(self, name: str, args: tuple):
+        self.name = name
+        self.fn = getattr(lib(), name)
+        self.args = args
+
+    def __call__(self, stream=None) -> None:
+        _check(self.name, self.fn(*self.args, _stream(stream)))
+
+
+def prepare_absorb_query(q, gamma_q, gamma_k, w_k, eps: float, q_tilde, alpha_q, plain: bool = False) -> Prepared:
+    """qkmla_absorb_query for fixed tensors (see absorb_query)."""
     rows, H, d_h = q.shape
     G, d_c, _ = w_k.shape
-    rc = lib().qkmla_absorb_query(_ptr(q), _ptr(gamma_q), _ptr(gamma_k), _ptr(w_k), rows, H, G, d_h, d_c,
-                                  float(eps), FLAG_PLAIN_MLA if plain else 0, _ptr(q_tilde),
-                                  _dtype_code(q_tilde.dtype), _ptr(alpha_q), _stream(stream))
-    _check("qkmla_absorb_query", rc)
+    return Prepared("qkmla_absorb_query",
+                    (_ptr(q), _ptr(gamma_q), _ptr(gamma_k), _ptr(w_k), rows, H, G, d_h, d_c, float(eps),
+                     FLAG_PLAIN_MLA if plain else 0, _ptr(q_tilde), _dtype_code(q_tilde.dtype), _ptr(alpha_q)))
+
+
+def absorb_query(q, gamma_q, gamma_k, w_k, eps: float, q_tilde, alpha_q, plain: bool = False, stream=None):
+    """q [rows, H, d_h] fp32 -> q_tilde [rows, H, d_c] (fp32/bf16), alpha_q [rows, H] fp32."""
+    prepare_absorb_query(q, gamma_q, gamma_k, w_k, eps, q_tilde, alpha_q, plain)(stream)
     return q_tilde, alpha_q
+
+
+def prepare_append(c_new, k_rope_new, w_k, gamma_rope_k, slot_mapping, kv_cache, ak_cache, eps: float,
+                   plain: bool = False) -> Prepared:
+    """qkmla_append for fixed tensors (see append)."""
+    N, d_c = c_new.shape
+    d_r = k_rope_new.shape[1]
+    G, _, d_h = w_k.shape
+    return Prepared("qkmla_append",
+                    (_ptr(c_new), _ptr(k_rope_new), _ptr(w_k), _ptr(gamma_rope_k), _ptr(slot_mapping), N, G, d_c,
+                     d_h, d_r, float(eps), FLAG_PLAIN_MLA if plain else 0, _ptr(kv_cache),
+                     _dtype_code(kv_cache.dtype), _ptr(ak_cache), kv_cache.shape[0]))
 
 
 def append(c_new, k_rope_new, w_k, gamma_rope_k, slot_mapping, kv_cache, ak_cache, eps: float,
            plain: bool = False, stream=None):
     """Write new tokens (c_new [N, d_c], k_rope_new [N, d_r], fp32) into kv_cache
     [num_slots, d_c+d_r] and ak_cache [num_slots, G] at slot_mapping [N] (int64)."""
-    N, d_c = c_new.shape
-    d_r = k_rope_new.shape[1]
-    G, _, d_h = w_k.shape
-    rc = lib().qkmla_append(_ptr(c_new), _ptr(k_rope_new), _ptr(w_k), _ptr(gamma_rope_k), _ptr(slot_mapping),
-                            N, G, d_c, d_h, d_r, float(eps), FLAG_PLAIN_MLA if plain else 0, _ptr(kv_cache),
-                            _dtype_code(kv_cache.dtype), _ptr(ak_cache), kv_cache.shape[0], _stream(stream))
-    _check("qkmla_append", rc)
+    prepare_append(c_new, k_rope_new, w_k, gamma_rope_k, slot_mapping, kv_cache, ak_cache, eps, plain)(stream)
 
 
 def make_decode_args(q_tilde, alpha_q, q_rope, gamma_rope_q, kv_cache, ak_cache, seq_lens, page_table,

@@ -11,12 +11,40 @@ import torch
 
 import workloads as W
 
-from . import (F32, BF16, absorb_query, append, decode_workspace_size, decode_raw, make_decode_args)
+from . import (F32, BF16, append, decode_workspace_size, decode_raw, make_decode_args, prepare_absorb_query,
+               prepare_append)
 
 _TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
 # quiet-NaN bit patterns written into untouched cache slots
 SENTINEL_BF16 = 0x7FC1
 SENTINEL_F32 = 0x7FC00001
+
+
+def packed(parts, device, empty=False):
+    """One device byte buffer holding the given arrays back to back (each part
+    256-byte aligned); returns the buffer and a tensor view of each part.  A step's
+    inputs (or outputs) then cross PCIe / C2C in a single copy.  With `empty` the
+    parts are (shape, dtype) pairs and the buffer is left unfilled."""
+    metas = []
+    off = 0
+    for part in parts:
+        if empty:
+            shape, dt = part
+            nbytes = int(np.prod(shape)) * torch.tensor([], dtype=dt).element_size()
+        else:
+            arr = np.ascontiguousarray(part)
+            shape, dt, nbytes = arr.shape, torch.from_numpy(arr[:0].copy()).dtype, arr.nbytes
+        off = (off + 255) & ~255
+        metas.append((off, shape, dt, nbytes, None if empty else arr))
+        off += nbytes
+    buf = torch.empty(max(off, 1), dtype=torch.uint8, device=device)
+    views = []
+    for o, shape, dt, nbytes, arr in metas:
+        v = buf[o:o + nbytes].view(dt).view(shape)
+        if arr is not None:
+            v.copy_(torch.from_numpy(arr))
+        views.append(v)
+    return buf, views
 
 
 def sentinel_fill(t: torch.Tensor) -> None:
@@ -57,13 +85,11 @@ class DeviceState:
         self.seq_lens = torch.from_numpy(self.lens.astype(np.int32)).to(d)
         self.page_table = torch.from_numpy(table).to(d) if self.paged else None
         q, qr = W.queries(w)
-        self.q_host, self.qr_host = q, qr
-        self.q = torch.from_numpy(q.reshape(w.rows, w.H, w.d_h)).to(d)
-        self.q_rope = torch.from_numpy(qr).to(d)
         self.q_tilde = torch.empty((w.B, w.s_q, w.H, w.d_c), dtype=cdt, device=d)
         self.alpha_q = torch.empty((w.B, w.s_q, w.H), dtype=torch.float32, device=d)
-        self.o = torch.empty((w.B, w.s_q, w.H, w.d_c), dtype=o_dtype, device=d)
-        self.lse = torch.empty((w.B, w.s_q, w.H), dtype=torch.float32, device=d)
+        # the step's results, o and lse, in one buffer
+        self.step_out, (self.o, self.lse) = packed(
+            [((w.B, w.s_q, w.H, w.d_c), o_dtype), ((w.B, w.s_q, w.H), torch.float32)], d, empty=True)
         # prefill, keeping the step's new tokens aside
         n_new = w.n_append
         new_c, new_r, new_slots = [], [], []
@@ -83,25 +109,36 @@ class DeviceState:
                 new_c.append(c[pre:])
                 new_r.append(r[pre:])
                 new_slots.append(W.slots_of(table, self.page_size, b, np.arange(pre, L)))
+        # the step's inputs -- queries, RoPE queries and the new tokens -- in one buffer
+        parts = [q.reshape(w.rows, w.H, w.d_h), qr]
         if n_new:
-            self.c_new = torch.from_numpy(np.concatenate(new_c)).to(d)
-            self.r_new = torch.from_numpy(np.concatenate(new_r)).to(d)
-            self.slots_new = torch.from_numpy(np.concatenate(new_slots)).to(d)
+            parts += [np.concatenate(new_c), np.concatenate(new_r), np.concatenate(new_slots).astype(np.int64)]
+        self.step_in, views = packed(parts, d)
+        self.q, self.q_rope = views[0], views[1]
+        if n_new:
+            self.c_new, self.r_new, self.slots_new = views[2], views[3], views[4]
         else:
             self.c_new = self.r_new = self.slots_new = None
         self.workspace = None
         self.args = None
+        self._absorb = self._append = None
 
     # -- the three calls -------------------------------------------------------
     def absorb(self, stream=None):
         w = self.w
-        absorb_query(self.q, self.gq, self.gk, self.wk, w.eps, self.q_tilde.view(w.rows, w.H, w.d_c),
-                     self.alpha_q.view(w.rows, w.H), plain=self.plain, stream=stream)
+        if self._absorb is None:             # the tensors never move: marshal once
+            self._absorb = prepare_absorb_query(self.q, self.gq, self.gk, self.wk, w.eps,
+                                                self.q_tilde.view(w.rows, w.H, w.d_c),
+                                                self.alpha_q.view(w.rows, w.H), plain=self.plain)
+        self._absorb(stream)
 
     def append_step(self, stream=None):
-        if self.c_new is not None:
-            append(self.c_new, self.r_new, self.wk, self.grk, self.slots_new, self.kv, self.ak, self.w.eps,
-                   plain=self.plain, stream=stream)
+        if self.c_new is None:
+            return
+        if self._append is None:
+            self._append = prepare_append(self.c_new, self.r_new, self.wk, self.grk, self.slots_new, self.kv,
+                                          self.ak, self.w.eps, plain=self.plain)
+        self._append(stream)
 
     def decode_args(self, num_splits: int = 0, force_simt: bool = False):
         w = self.w
