@@ -4,6 +4,10 @@ Argument marshalling only: every step of the decode path runs in the CUDA
 kernels behind the C ABI declared in include/qkmla.h.  PyTorch provides device
 memory and streams.  There is no fallback: if the shared library is missing
 or a call fails, an exception is raised.
+
+Calls: absorb_query, append, decode (or make_decode_args + decode_raw to keep
+one argument block); prepare_absorb_query / prepare_append return a Prepared
+call whose arguments are marshalled once, for loops over fixed buffers.
 """
 from __future__ import annotations
 
