@@ -179,8 +179,9 @@ def cpu_oracle_rate(w: W.Workload, target_s: float):
     lens = W.seq_lens(w)
     order = [int(b) for b in np.argsort(lens)]   # shortest first: bounded sample
     t_total, done, toks = 0.0, [], 0
-    # passes over the batch (shortest sequence first) until about target_s seconds
-    while t_total < target_s:
+    # passes over the batch (shortest sequence first) until about target_s seconds,
+    # at least one sequence step
+    while not done or t_total < target_s:
         for b in order:
             c, r = W.sequence(w, b)
             t0 = time.perf_counter()

@@ -58,3 +58,11 @@ def test_code_hash_ignores_comments_and_layout(tmp_path):
     assert bench.kernel_signature(str(dst)) == base        # comments and blank lines only
     f.write_text(text.replace("constexpr int kThreads = 192;", "constexpr int kThreads = 256;"))
     assert bench.kernel_signature(str(dst)) != base        # a code change
+
+
+def test_cpu_baseline_always_times_at_least_one_sequence():
+    # the reference arm's warm-up asks for a zero-second sample
+    w = W.small(W.WORKLOADS[0], 1, (64,))
+    rate, sample, secs = bench.cpu_oracle_rate(w, 0.0)
+    assert rate > 0 and secs > 0
+    assert sample.startswith("1 sequence steps")
