@@ -39,7 +39,10 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", type=int, default=1, help="index into workloads.WORKLOADS")
+    ap.add_argument("--workload", type=int, default=4,
+                    help="index into workloads.WORKLOADS (default 4: B=128, s_q=2, the largest single-GPU workload)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="keep only the first N sequences of the workload (a reduced case for profiling)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-plain", action="store_true", help="skip the plain-MLA comparator timing")
@@ -171,24 +174,28 @@ def kernel_signature(csrc=None):
 # ----------------------------------------------------------------------------
 def cpu_oracle_rate(w: W.Workload, target_s: float):
     """Time the oracle's whole path (absorb, append of the sequence, explicit
-    decode) on whole sequences until about target_s seconds of work.  Returns
-    (tokens/s, sample description, threads)."""
+    decode) on whole sequences until about target_s seconds of work, in this one
+    Python process (numpy; its BLAS may run the matrix products on several
+    threads).  Returns (tokens/s, sample description, seconds, threads busy on
+    average = process CPU time / wall time)."""
     import oracle as O
     wk, gq, gk, grq, grk = W.weights(w)
     q, qr = W.queries(w)
     lens = W.seq_lens(w)
     order = [int(b) for b in np.argsort(lens)]   # shortest first: bounded sample
-    t_total, done, toks = 0.0, [], 0
+    t_total, cpu_total, done, toks = 0.0, 0.0, [], 0
     # passes over the batch (shortest sequence first) until about target_s seconds,
     # at least one sequence step
     while not done or t_total < target_s:
         for b in order:
             c, r = W.sequence(w, b)
             t0 = time.perf_counter()
+            c0 = time.process_time()
             ch, rh, ak = O.append_tokens(c, r, wk, grk, w.eps, w.cache_dtype)
             O.absorb_query(q[b].reshape(w.s_q, w.H, w.d_h), gq, gk, wk, w.eps)
             O.decode_explicit(q[b:b + 1], qr[b:b + 1], gq, gk, grq, wk, [(ch, rh)], w.s_q, w.scale, w.eps)
             t_total += time.perf_counter() - t0
+            cpu_total += time.process_time() - c0
             done.append(b)
             toks += w.s_q
             if t_total >= target_s:
@@ -197,7 +204,7 @@ def cpu_oracle_rate(w: W.Workload, target_s: float):
     sample = (f"{len(done)} sequence steps over the {w.B} sequences ({len(done) / w.B:.2f} passes, {ctx} cached "
               f"tokens in all), whole path: oracle append of the sequence (alpha^k over all groups), absorb, "
               f"explicit decode with materialised keys")
-    return toks / t_total, sample, t_total
+    return toks / t_total, sample, t_total, cpu_total / max(t_total, 1e-9)
 
 
 def rank_workload(w0: W.Workload, rank: int) -> W.Workload:
@@ -222,6 +229,15 @@ def job_throughput(units_per_rank_step: int, world: int, total_ms_max: float, st
     return units_per_rank_step * world * steps / (total_ms_max / 1e3)
 
 
+def config_of(w: W.Workload, lens: np.ndarray, world: int) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": w.name, "B": w.B, "s_q": w.s_q, "H": w.H, "G": w.G, "d_c": w.d_c,
+            "d_h": w.d_h, "d_r": w.d_r, "cache": w.cache_dtype,
+            "context_tokens": int(np.asarray(lens).sum()), "n_append_per_seq": w.n_append,
+            "page_size": w.page_size, "parallelism": f"dp{world} (replicas, no collective)",
+            "l2": "flushed before every step (256 MiB fill outside the timed intervals)"}
+
+
 def cpu_threads() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -236,6 +252,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     w0 = W.WORKLOADS[args.workload]
+    if 0 < args.batch < w0.B:
+        w0 = W.small(w0, args.batch, W.seq_lens(w0)[:args.batch], name=f"{w0.name}_first{args.batch}")
 
     if args.impl == "reference":
         if rank != 0:
@@ -244,18 +262,21 @@ def main():
         step_rates = []
         for _ in range(args.warmup):
             cpu_oracle_rate(W.small(w0, 1, (min(256, int(W.seq_lens(w0).min())),)), 0.0)
+        busy = []
         for _ in range(max(1, args.steps)):
-            r_, sample, secs = cpu_oracle_rate(w0, args.cpu_seconds / max(1, args.steps))
+            r_, sample, secs, busy_ = cpu_oracle_rate(w0, args.cpu_seconds / max(1, args.steps))
+            busy.append(busy_)
             step_rates.append(r_)
         rate = statistics.median(step_rates)
         line = {"impl": "reference", "metric": "decode tokens/s", "value": rate, "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1000.0 * w0.B * w0.s_q / rate, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": w0.name, "B": w0.B, "s_q": w0.s_q, "H": w0.H, "G": w0.G, "d_c": w0.d_c,
-                           "d_h": w0.d_h, "d_r": w0.d_r, "cache": w0.cache_dtype},
-                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-                                 "sample": sample + " per step"},
+                "config": config_of(w0, W.seq_lens(w0), args.gpus),
+                "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": max(1, round(statistics.mean(busy))),
+                                 "cores_available": cpu_threads(), "kind": "oracle",
+                                 "sample": sample + " per step; one Python process (numpy fp64; cores = its "
+                                           "CPU time / wall time, the BLAS threads of the matrix products)"},
                 "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return 0
@@ -358,6 +379,11 @@ def main():
     roof["kernel"] = f"qkmla_decode[{kernel}]"
     roof["algorithmic_bytes_per_launch"] = bytes_alg
     roof["algorithmic_flops_per_launch"] = flops_alg
+    roof["flops_rule"] = "per (query token, visible cached token, head): 2 (d_c + d_r) logit + 2 d_c output"
+    if roof["bound"] == "tensor":
+        # the decode call is timed alone (graph replays back to back): the burst peak; the
+        # sustained figure is given beside it
+        roof["frac_of_sustained"] = roof["achieved"] / pk["bf16_tflops_sustained"]
     roof["roofline_us"] = max(t_hbm, t_mma) * 1e6
 
     # plain-MLA comparator: same kernels with the alpha scaling off
@@ -400,8 +426,11 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, sample, secs = cpu_oracle_rate(w, args.cpu_seconds)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample,
+        rate, sample, secs, busy = cpu_oracle_rate(w, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": max(1, round(busy)), "cores_available": cpu_threads(),
+               "kind": "oracle",
+               "sample": sample + "; one Python process (numpy fp64; cores = its CPU time / wall time, the BLAS "
+                                  "threads of the matrix products)",
                "seconds": secs}
 
     if rank == 0:
@@ -410,14 +439,9 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.cache_dtype,
             "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "s_q": w.s_q, "H": w.H, "G": w.G, "d_c": w.d_c,
-                       "d_h": w.d_h, "d_r": w.d_r, "cache": w.cache_dtype,
-                       "context_tokens": int(lens.sum()), "n_append_per_seq": w.n_append,
-                       "page_size": w.page_size, "parallelism": f"dp{world} (replicas, no collective)",
-                       "l2": "flushed before every step (256 MiB fill outside the timed intervals)",
-                       "launch": "each step replays a CUDA graph of absorb, append and the decode call; "
-                                 "decode_ms and the roofline replay a graph of the decode call alone; "
-                                 "e2e drives the Python API call by call"},
+            "config": config_of(w, lens, world),
+            "launch": "each step replays a CUDA graph of absorb, append and the decode call; decode_ms and the "
+                      "roofline replay a graph of the decode call alone; e2e drives the Python API call by call",
             "decode_ms": dec_avg,
             "kv_gbs": bytes_alg / (dec_avg * 1e-3) / 1e9,
             "roofline": roof,

@@ -71,7 +71,14 @@ enum {
     QKMLA_FLAG_PLAIN_MLA = 1u,
     /* Decode: force the CUDA-core (SIMT) kernel even where the tensor-core
      * kernel applies.  Used to cross-check the two kernels. */
-    QKMLA_FLAG_FORCE_SIMT = 2u
+    QKMLA_FLAG_FORCE_SIMT = 2u,
+    /* Decode, test hook for the failure path: the 64-row tensor-core kernel's
+     * loader issues no tile from the second one on and every wait gives up
+     * after 1 ms, so a call whose sequences span two or more tiles ends with
+     * QKMLA_ERR_TIMEOUT in the status word (outputs undefined) and leaves the
+     * context usable.  QKMLA_ERR_UNSUPPORTED for arguments that select another
+     * kernel.  Never set outside tests. */
+    QKMLA_FLAG_TEST_STALL = 4u
 };
 
 /*

@@ -22,6 +22,7 @@ OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE_BOUNDS, ER
 F32, BF16 = 0, 1
 FLAG_PLAIN_MLA = 1
 FLAG_FORCE_SIMT = 2
+FLAG_TEST_STALL = 4
 
 SYMBOLS = [
     "qkmla_absorb_query", "qkmla_append", "qkmla_decode_workspace_size", "qkmla_decode",

@@ -71,13 +71,16 @@ int plan_decode(const qkmla_decode_args* a, DecodePlan* plan) {
     if (v != QKMLA_OK) return v;
     const int sms = device_sm_count();
     if (sms <= 0) return QKMLA_ERR_CUDA;
+    const bool stall = (a->flags & QKMLA_FLAG_TEST_STALL) != 0;
     if (!(a->flags & QKMLA_FLAG_FORCE_SIMT) && tc_supported(a) && a->num_splits <= 256) {
+        if (stall && pair_shape(a)) return QKMLA_ERR_UNSUPPORTED;   // the hook exists in the 64-row kernel only
         plan->kernel = 1;
         plan->num_splits = a->num_splits;
         plan->parts = 0;
         plan->ws_bytes = tc_workspace(a, sms, nullptr);
         return QKMLA_OK;
     }
+    if (stall) return QKMLA_ERR_UNSUPPORTED;
     plan->kernel = 0;
     int ns = a->num_splits;
     if (ns == 0) {

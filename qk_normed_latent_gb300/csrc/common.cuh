@@ -105,6 +105,7 @@ int plan_decode(const qkmla_decode_args* a, DecodePlan* plan);
 int launch_decode_simt(const qkmla_decode_args* a, const DecodePlan& plan, cudaStream_t s);
 int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStream_t s);
 bool tc_supported(const qkmla_decode_args* a);
+bool pair_shape(const qkmla_decode_args* a);        // served by the two-CTA cluster kernel
 bool sched_in_kernel(const qkmla_decode_args* a);   // split plan computed by the decode kernels themselves
 size_t tc_workspace(const qkmla_decode_args* a, int sms, int* max_items_out);
 int launch_combine(const float* o_part, const float* lse_part, int rows, int nsplit, int d_c, void* o,

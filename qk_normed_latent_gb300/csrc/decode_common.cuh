@@ -50,6 +50,8 @@ struct TcParams {
     int o_dtype;
     float* lse;
     int* status;
+    uint64_t wait_ns;          // bound on any single wait (64-row kernel)
+    int withhold_tile;         // test hook (64-row kernel): the producer issues no tile from this one on; -1 off
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -58,13 +60,15 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
-// Bounded wait: spins on try_wait, checks the wall clock every 256 polls.
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
+// Bounded wait: spins on try_wait, checks the wall clock every 256 polls and
+// gives up (recording QKMLA_ERR_TIMEOUT) after limit_ns.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, int* status,
+                                             uint64_t limit_ns = kWaitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && globaltimer() - t0 > kWaitNs) {
+        if ((i & 255u) == 0 && globaltimer() - t0 > limit_ns) {
             report(status, QKMLA_ERR_TIMEOUT);
             return false;
         }

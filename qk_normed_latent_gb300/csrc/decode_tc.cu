@@ -149,6 +149,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
     const int jt1 = min(it.tile_end, tiles);
     const int n_t = max(0, jt1 - jt0);
     const int hpg = p.H / p.G;
+    // tiles the producer issues: all of them, or (test hook) those before the
+    // withheld one -- the consumers' waits for the next tile then run out
+    const int n_issue = p.withhold_tile >= 0 ? min(n_t, p.withhold_tile) : n_t;
 
     if (tid == 0) {
         if (bad) report(p.status, QKMLA_ERR_DEVICE_BOUNDS);
@@ -207,7 +210,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             for (int blk = 0; blk < LY::kLatBlocks; ++blk)
                 tma_load_2d(sQ + blk * (kRowsMMA * 128), &tm_q, blk * 64, (int)qrow0, qfull);
         }
-        for (int j = 0; j < NST && j < n_t; ++j) {
+        for (int j = 0; j < NST && j < n_issue; ++j) {
             const int64_t slot0 = __shfl_sync(0xffffffffu, slot_batch, j);
             if (lane == 0) issue_tile(j, slot0);
         }
@@ -259,13 +262,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
 
     if (warp == 0) {
         // ===================== TMA producer (lane 0 issues; lanes hold page slots) =====================
-        for (int j = NST; j < n_t; ++j) {
+        for (int j = NST; j < n_issue; ++j) {
             if ((j & 31) == 0) slot_batch = slot_of_tile(j + lane);
             const int64_t slot0 = __shfl_sync(0xffffffffu, slot_batch, j & 31);
             int go = 1;
             if (lane == 0) {
                 const int s = j % NST;
-                if (!wait_bounded(&empty[s], ((j / NST) - 1) & 1, p.status)) {
+                if (!wait_bounded(&empty[s], ((j / NST) - 1) & 1, p.status, p.wait_ns)) {
                     *abort_flag = 1;
                     go = 0;
                 } else if (*(volatile int*)abort_flag) {
@@ -284,7 +287,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             const uint32_t q_addr = smem_u32(sQ);
             auto issue_o = [&](int jj) -> bool {
                 const int s = jj % NST;
-                if (!wait_bounded(&pfull[s], (jj / NST) & 1, p.status)) return false;
+                if (!wait_bounded(&pfull[s], (jj / NST) & 1, p.status, p.wait_ns)) return false;
                 tc_fence_after();
                 const uint32_t st_addr = smem_u32(sm + LY::kOffStage + s * LY::kStage);
                 const uint32_t p_addr = st_addr + LY::kSLat;       // P^T lives in the RoPE slot
@@ -308,11 +311,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                 return true;
             };
             // always waited, so no CTA exits with the Q~ copy in flight
-            bool ok = wait_bounded(qfull, 0, p.status);
+            bool ok = wait_bounded(qfull, 0, p.status, p.wait_ns);
             for (int j = 0; j < n_t && ok; ++j) {
                 const int s = j % NST, sb = j % NSB;
-                if (!wait_bounded(&full[s], (j / NST) & 1, p.status)) { ok = false; break; }
-                if (j >= NSB && !wait_bounded(&sfree[sb], ((j / NSB) - 1) & 1, p.status)) { ok = false; break; }
+                if (!wait_bounded(&full[s], (j / NST) & 1, p.status, p.wait_ns)) { ok = false; break; }
+                if (j >= NSB && !wait_bounded(&sfree[sb], ((j / NSB) - 1) & 1, p.status, p.wait_ns)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t st_addr = smem_u32(sm + LY::kOffStage + s * LY::kStage);
                 const uint32_t d_c = tmem + LY::kColSc + sb * KT;
@@ -373,7 +376,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             // a timed-out wait is folded into the per-tile vote below, so every abort
             // decision is uniform across the four softmax warps (none is left at a
             // named barrier)
-            const bool got_s = wait_bounded(&sfull[sb], (j / NSB) & 1, p.status);
+            const bool got_s = wait_bounded(&sfull[sb], (j / NSB) & 1, p.status, p.wait_ns);
             if (!got_s) *(volatile int*)abort_flag = 1;
             tc_fence_after();
             uint8_t* stg = sm + LY::kOffStage + s * LY::kStage;
@@ -422,7 +425,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             bool o_seen = (j == 0);
             if (any) {
                 // rescale O^T columns (rows) in TMEM once the previous output MMA is done
-                const bool got_o = wait_bounded(odone, (j - 1) & 1, p.status);
+                const bool got_o = wait_bounded(odone, (j - 1) & 1, p.status, p.wait_ns);
                 if (named_bar_any(!got_o)) { ok = false; break; }
                 o_seen = true;
                 tc_fence_after();
@@ -478,7 +481,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                         make_uint4(0, 0, 0, 0);
                 }
             }
-            if (!o_seen && !wait_bounded(odone, (j - 1) & 1, p.status)) {
+            if (!o_seen && !wait_bounded(odone, (j - 1) & 1, p.status, p.wait_ns)) {
                 *(volatile int*)abort_flag = 1;
                 late_fail = true;           // acted on, uniformly, at the next tile's vote
             }
@@ -490,7 +493,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
         // the two halves of a row hold partial sums
         l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
         // ---- epilogue ----
-        const bool got_last = (ok && n_t > 0) ? wait_bounded(odone, (n_t - 1) & 1, p.status) : true;
+        const bool got_last = (ok && n_t > 0) ? wait_bounded(odone, (n_t - 1) & 1, p.status, p.wait_ns) : true;
         if (named_bar_any(!got_last)) ok = false;
         tc_fence_after();
         if (!ok) *(volatile int*)abort_flag = 1;
@@ -914,6 +917,11 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     tp.o_dtype = a->o_dtype;
     tp.lse = a->lse;
     tp.status = status;
+    // test hook: withhold the second tile and give up waiting after 1 ms (64-row kernel only;
+    // plan_decode rejects the flag for the other kernels)
+    const bool stall = (a->flags & QKMLA_FLAG_TEST_STALL) != 0;
+    tp.wait_ns = stall ? 1000000ull : kWaitNs;
+    tp.withhold_tile = stall ? 1 : -1;
     const bool plain = (a->flags & QKMLA_FLAG_PLAIN_MLA) != 0;
     int rc;
     if (pair_shape(a)) {

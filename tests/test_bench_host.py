@@ -8,6 +8,8 @@ import numpy as np
 import bench
 import workloads as W
 
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
 
 def test_bytes_per_cached_token():
     # a cached token is its latent + RoPE row in the cache dtype plus G fp32 alpha^k
@@ -63,6 +65,23 @@ def test_code_hash_ignores_comments_and_layout(tmp_path):
 def test_cpu_baseline_always_times_at_least_one_sequence():
     # the reference arm's warm-up asks for a zero-second sample
     w = W.small(W.WORKLOADS[0], 1, (64,))
-    rate, sample, secs = bench.cpu_oracle_rate(w, 0.0)
+    rate, sample, secs, busy = bench.cpu_oracle_rate(w, 0.0)
     assert rate > 0 and secs > 0
     assert sample.startswith("1 sequence steps")
+    assert busy > 0
+
+
+def test_reference_arm_reports_the_same_config():
+    """Both arms print the same `config` object for a workload, so the driver can
+    pair them."""
+    import json
+    import subprocess
+    import sys
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "0",
+                          "--steps", "1", "--warmup", "0", "--cpu-seconds", "0.05"],
+                         capture_output=True, text=True, check=True).stdout
+    line = json.loads(out.strip().splitlines()[-1])
+    w = W.WORKLOADS[0]
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.config_of(w, W.seq_lens(w), 1)
+    assert line["cpu_baseline"]["cores"] >= 1

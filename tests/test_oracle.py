@@ -104,15 +104,34 @@ def test_inv_rms_matches_torch_rms_norm():
 # --------------------------------------------------------------------------
 # explicit definition vs torch library attention (textbook reduction)
 # --------------------------------------------------------------------------
-def _torch_reference(case, exp_seqs, plain=False):
+def _torch_cache(x, cache):
+    """A value as the cache stores it, by torch's own casts (fp64 -> fp32 -> cache dtype)."""
+    t = torch.as_tensor(x).to(torch.float32)
+    if cache == "bf16":
+        t = t.to(torch.bfloat16)
+    return t.to(torch.float64)
+
+
+def _torch_rope_key(r, gamma, eps, cache, plain=False):
+    """Stored RoPE key built with torch's rms_norm from the raw key (not from the oracle)."""
+    rt = torch.from_numpy(np.asarray(r, np.float64))
+    if not plain:
+        rt = F.rms_norm(rt, (rt.shape[-1],), torch.from_numpy(np.asarray(gamma, np.float64)), eps=eps)
+    return _torch_cache(rt, cache)
+
+
+def _torch_reference(case, plain=False):
     """Post-projection QK RMSNorm attention with torch's rms_norm and
-    scaled_dot_product_attention (fp64, CPU)."""
+    scaled_dot_product_attention (fp64, CPU), built from the raw inputs: the
+    stored latent and RoPE key come from torch's casts and rms_norm, not from
+    the oracle's append."""
     B, s_q, H, G = case["B"], case["s_q"], case["H"], case["G"]
     hpg = H // G
     o_all = np.zeros((B, s_q, H, case["d_c"]))
     for b in range(B):
-        ch = torch.from_numpy(exp_seqs[b][0])
-        rh = torch.from_numpy(exp_seqs[b][1])
+        c_raw, r_raw = case["seqs_raw"][b]
+        ch = _torch_cache(torch.from_numpy(c_raw), case["cache"])
+        rh = _torch_rope_key(r_raw, case["grk"], case["eps"], case["cache"], plain)
         T = ch.shape[0]
         for h in range(H):
             g_ = h // hpg
@@ -141,7 +160,7 @@ def test_explicit_matches_torch_sdpa(s_q, plain):
     exp_seqs, _ = _build(case, plain=plain)
     o, _ = O.decode_explicit(case["q"], case["qr"], case["gq"], case["gk"], case["grq"], case["wk"],
                              exp_seqs, s_q, case["scale"], case["eps"], plain=plain)
-    ref = _torch_reference(case, exp_seqs, plain=plain)
+    ref = _torch_reference(case, plain=plain)
     np.testing.assert_allclose(o, ref, rtol=1e-11, atol=1e-11)
 
 
@@ -175,16 +194,20 @@ def test_single_token_returns_its_latent():
     exp_seqs, _ = _build(case)
     o, lse = O.decode_explicit(case["q"], case["qr"], case["gq"], case["gk"], case["grq"], case["wk"],
                                exp_seqs, 1, case["scale"], case["eps"])
-    ch, rh = exp_seqs[0]
-    np.testing.assert_allclose(o[0, 0], np.broadcast_to(ch[0], o[0, 0].shape), rtol=0, atol=1e-14)
+    c_raw, r_raw = case["seqs_raw"][0]
+    c0 = c_raw[0].astype(np.float64)                      # fp32 cache: the stored latent is the input
+    np.testing.assert_allclose(o[0, 0], np.broadcast_to(c0, o[0, 0].shape), rtol=0, atol=1e-14)
+    # the stored RoPE key, by hand: r gamma_rk / sqrt(mean r^2 + eps), stored in fp32
+    r0 = r_raw[0].astype(np.float64)
+    rk = (r0 * case["grk"] / math.sqrt(np.mean(r0 * r0) + case["eps"])).astype(np.float32).astype(np.float64)
     # lse = the single logit, computed by hand for head 0 (group 0)
-    k = ch[0] @ case["wk"][0].astype(np.float64)
+    k = c0 @ case["wk"][0].astype(np.float64)
     kh = k * case["gk"] / math.sqrt(np.mean(k * k) + case["eps"])
     qh = case["q"][0, 0, 0].astype(np.float64)
     qh = qh * case["gq"] / math.sqrt(np.mean(qh * qh) + case["eps"])
     qrh = case["qr"][0, 0, 0].astype(np.float64)
     qrh = qrh * case["grq"] / math.sqrt(np.mean(qrh * qrh) + case["eps"])
-    ell = case["scale"] * (float(qh @ kh) + float(qrh @ rh[0]))
+    ell = case["scale"] * (float(qh @ kh) + float(qrh @ rk))
     assert lse[0, 0, 0] == pytest.approx(ell, rel=1e-13, abs=1e-13)
 
 
@@ -408,6 +431,33 @@ def test_mutation_eps_outside_root_is_caught(monkeypatch):
     o, _ = O.decode_explicit(case["q"], case["qr"], case["gq"], case["gk"], case["grq"], case["wk"],
                              exp_seqs, 1, case["scale"], case["eps"])
     monkeypatch.setattr(O.qkmla_oracle, "inv_rms", real)
-    exp_ok, _ = _build(case)
-    ref = _torch_reference(case, exp_ok)
+    ref = _torch_reference(case)
     assert np.max(np.abs(o - ref)) > 1e-4
+
+
+@pytest.mark.parametrize("cache", ["f32", "bf16"])
+@pytest.mark.parametrize("mutation", ["dropped_gamma_rk", "key_scaled_1.05", "norm_over_wrong_axis"])
+def test_mutation_rope_key_is_caught(monkeypatch, cache, mutation):
+    """The stored RoPE key is pinned by the torch reference built from the raw key:
+    a dropped RoPE gamma, a mis-scaled key or a statistic over the wrong axis in
+    the oracle's rope_key must move the explicit decode away from it."""
+    real = O.qkmla_oracle.rope_key
+    bad = {
+        "dropped_gamma_rk": lambda r, g, eps, c, plain=False: real(r, None, eps, c, plain),
+        "key_scaled_1.05": lambda r, g, eps, c, plain=False: real(r, g, eps, c, plain) * 1.05,
+        "norm_over_wrong_axis": lambda r, g, eps, c, plain=False: O.cache_cast(
+            (np.asarray(r, np.float64) * np.asarray(g, np.float64)
+             * O.inv_rms(np.asarray(r, np.float64).T, eps)[None, :]).astype(np.float32), c),
+    }[mutation]
+    case = _rand_case(62, B=2, lens=(40, 57), cache=cache)
+    ref = _torch_reference(case)
+
+    def gap():
+        exp_seqs, _ = _build(case)
+        o, _ = O.decode_explicit(case["q"], case["qr"], case["gq"], case["gk"], case["grq"], case["wk"],
+                                 exp_seqs, 1, case["scale"], case["eps"])
+        return np.max(np.abs(o - ref))
+
+    assert gap() < 1e-11
+    monkeypatch.setattr(O.qkmla_oracle, "rope_key", bad)
+    assert gap() > 1e-5

@@ -50,6 +50,7 @@ class Workload:
     n_append: int             # new latents appended per sequence inside one step
     seed: int
     eps: float = 1e-6
+    rope_gamma_std: float = 0.0   # RoPE gammas = 1 + std * N(0,1) (0: ones, the pages name none)
 
     @property
     def scale(self) -> float:
@@ -100,13 +101,19 @@ def seq_lens(w: Workload) -> np.ndarray:
 
 def weights(w: Workload):
     """W^K [G, d_c, d_h] ~ N(0, 1/d_c); gamma_q, gamma_k [d_h] = 1 + 0.1 N(0,1);
-    RoPE gammas [d_r] = ones.  All fp32."""
+    RoPE gammas [d_r] = ones, or 1 + rope_gamma_std N(0,1) from a stream of
+    their own (so the other draws do not change).  All fp32."""
     g = _rng(w.seed, 0)
     wk = (g.standard_normal((w.G, w.d_c, w.d_h), dtype=np.float32) / np.float32(math.sqrt(w.d_c))).astype(np.float32)
     gq = (1.0 + 0.1 * g.standard_normal(w.d_h, dtype=np.float32)).astype(np.float32)
     gk = (1.0 + 0.1 * g.standard_normal(w.d_h, dtype=np.float32)).astype(np.float32)
-    grq = np.ones(w.d_r, dtype=np.float32)
-    grk = np.ones(w.d_r, dtype=np.float32)
+    if w.rope_gamma_std > 0:
+        gr = _rng(w.seed, 5)
+        grq = (1.0 + w.rope_gamma_std * gr.standard_normal(w.d_r, dtype=np.float32)).astype(np.float32)
+        grk = (1.0 + w.rope_gamma_std * gr.standard_normal(w.d_r, dtype=np.float32)).astype(np.float32)
+    else:
+        grq = np.ones(w.d_r, dtype=np.float32)
+        grk = np.ones(w.d_r, dtype=np.float32)
     return wk, gq, gk, grq, grk
 
 
