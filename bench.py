@@ -62,7 +62,7 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def algorithmic(w: W.Workload, lens: np.ndarray, plain: bool = False):
+def algorithmic(w: W.Workload, lens: np.ndarray, plain: bool = False, alpha_bytes: int = 4):
     """Algorithmic bytes and MMA flops of one decode call.
 
     Bytes: every cached token's row (latent + RoPE key) once, its G alpha^k
@@ -72,7 +72,7 @@ def algorithmic(w: W.Workload, lens: np.ndarray, plain: bool = False):
     """
     cb = 4 if w.cache_dtype == "f32" else 2
     tokens = int(lens.sum())
-    kv_bytes = tokens * (w.d_c + w.d_r) * cb + (0 if plain else tokens * w.G * 4)
+    kv_bytes = tokens * (w.d_c + w.d_r) * cb + (0 if plain else tokens * w.G * alpha_bytes)
     rows = w.B * w.s_q * w.H
     q_bytes = rows * (w.d_c * cb + 4 + w.d_r * 4)
     o_bytes = rows * (w.d_c * 4 + 4)
@@ -386,21 +386,37 @@ def main():
         roof["frac_of_sustained"] = roof["achieved"] / pk["bf16_tflops_sustained"]
     roof["roofline_us"] = max(t_hbm, t_mma) * 1e6
 
-    # plain-MLA comparator: same kernels with the alpha scaling off
+    # plain-MLA comparator: same kernels with the alpha scaling off; and the same QK-norm
+    # path with the scalar cache in fp16 (half the alpha^k bytes)
     plain = None
+    alpha_f16 = None
     if not args.no_plain:
         sp = DeviceState(w, plain=True)
+        sb = DeviceState(w.with_(alpha_dtype="f16"))
         for _ in range(3):
             sp.step()
+            sb.step()
         torch.cuda.synchronize()
+        if Q.get_device_status() != 0:
+            raise RuntimeError("device status error in the comparator warm-up")
         sp_step_g, sp_dec_g = graphs_of(sp)
+        sb_step_g, sb_dec_g = graphs_of(sb)
         kp = min(args.steps, 100)
         p_step, p_dec = timed(sp_step_g, kp), timed(sp_dec_g, kp)
         q_step, q_dec = timed(step_graph, kp), timed(dec_graph, kp)
-        plain = {"decode_ms": statistics.median(p_dec), "qknorm_decode_ms": statistics.median(q_dec),
-                 "overhead_pct": 100.0 * (statistics.median(q_dec) / statistics.median(p_dec) - 1.0),
-                 "step_overhead_pct": 100.0 * (statistics.median(q_step) / statistics.median(p_step) - 1.0)}
-        del sp_step_g, sp_dec_g, sp
+        b_step, b_dec = timed(sb_step_g, kp), timed(sb_dec_g, kp)
+        med = statistics.median
+        plain = {"decode_ms": med(p_dec), "qknorm_decode_ms": med(q_dec),
+                 "overhead_pct": 100.0 * (med(q_dec) / med(p_dec) - 1.0),
+                 "step_overhead_pct": 100.0 * (med(q_step) / med(p_step) - 1.0)}
+        bytes_b, _, _ = algorithmic(w, lens, alpha_bytes=2)
+        alpha_f16 = {"decode_ms": med(b_dec), "overhead_vs_plain_pct": 100.0 * (med(b_dec) / med(p_dec) - 1.0),
+                      "step_overhead_vs_plain_pct": 100.0 * (med(b_step) / med(p_step) - 1.0),
+                      "kv_gbs": bytes_b / (med(b_dec) * 1e-3) / 1e9,
+                      "byte_floor_pct": 100.0 * (w.G * 2) / ((w.d_c + w.d_r) * (4 if w.cache_dtype == "f32" else 2))}
+        if Q.get_device_status() != 0:
+            raise RuntimeError("device status error in the comparator timing")
+        del sp_step_g, sp_dec_g, sp, sb_step_g, sb_dec_g, sb
 
     # end to end through the public API with host buffers: H2D of the step's inputs,
     # the three calls, D2H of o and lse, all inside the timed region.  The inputs
@@ -446,6 +462,7 @@ def main():
             "kv_gbs": bytes_alg / (dec_avg * 1e-3) / 1e9,
             "roofline": roof,
             "plain_mla": plain,
+            "alpha_f16": alpha_f16,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,

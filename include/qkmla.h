@@ -30,7 +30,8 @@
  *    (rows = B*s_q), H query heads, G KV groups with g(h) = h / (H/G),
  *    d_h head dim of the content (nope) part, d_c latent dim, d_r RoPE dim.
  *  - Cache: one flat array of slots.  kv_cache[slot] = [c_t (d_c) | k^rope_t
- *    (d_r)] in the cache dtype; ak_cache[slot] = [alpha^k_{t,0..G-1}] fp32.
+ *    (d_r)] in the cache dtype; ak_cache[slot] = [alpha^k_{t,0..G-1}] fp32
+ *    (fp16 with QKMLA_FLAG_ALPHA_F16).
  *    Token t of sequence b lives in slot
  *        page_table[b*max_pages + t/page_size]*page_size + t%page_size,
  *    and with page_table == NULL in slot (b*max_pages + t/page_size)*page_size
@@ -78,7 +79,16 @@ enum {
      * QKMLA_ERR_TIMEOUT in the status word (outputs undefined) and leaves the
      * context usable.  QKMLA_ERR_UNSUPPORTED for arguments that select another
      * kernel.  Never set outside tests. */
-    QKMLA_FLAG_TEST_STALL = 4u
+    QKMLA_FLAG_TEST_STALL = 4u,
+    /* Append and decode: A^k_cache holds IEEE half-precision scalars
+     * ([num_slots][G], 2 bytes each, round-to-nearest-even of the fp32
+     * alpha^k) instead of fp32.  Halves the scalar cache, the method's only
+     * storage overhead over MLA (Technical Summary, Key Contributions and
+     * Results).  alpha^k = 1/sqrt(mean k^2 + eps) stays in fp16's normal range
+     * (6.1e-5 .. 65504) for key RMS up to ~16000 and eps down to 2.3e-10; 11
+     * significant bits keep each content logit within 2^-11 of its fp32 value.
+     * Ignored with QKMLA_FLAG_PLAIN_MLA. */
+    QKMLA_FLAG_ALPHA_F16 = 8u
 };
 
 /*
@@ -117,7 +127,8 @@ int qkmla_absorb_query(const float* q, const float* gamma_q, const float* gamma_
  *                    beta_n = 1 / sqrt(mean_j k_rope_new[n][j]^2 + eps)
  * c_new [N][d_c] fp32, k_rope_new [N][d_r] fp32 (post-RoPE), w_k as above,
  * gamma_rope_k [d_r] fp32 or NULL (ones), slot_mapping [N] int64 device.
- * kv_cache [num_slots][d_c+d_r] in cache_dtype, ak_cache [num_slots][G] fp32.
+ * kv_cache [num_slots][d_c+d_r] in cache_dtype, ak_cache [num_slots][G] fp32
+ * (fp16, the RNE cast of the fp32 value, with QKMLA_FLAG_ALPHA_F16).
  * PLAIN_MLA: the raw RoPE key is stored and ak = 1.
  * A slot >= num_slots is a device-side bounds error (skipped, status set).
  * N == 0 is a no-op.  Errors: INVALID / UNSUPPORTED as for absorb; d_h <= 256.
@@ -125,7 +136,7 @@ int qkmla_absorb_query(const float* q, const float* gamma_q, const float* gamma_
 int qkmla_append(const float* c_new, const float* k_rope_new, const float* w_k,
                  const float* gamma_rope_k, const int64_t* slot_mapping, int N, int G,
                  int d_c, int d_h, int d_r, float eps, unsigned flags, void* kv_cache,
-                 int cache_dtype, float* ak_cache, int64_t num_slots, void* stream);
+                 int cache_dtype, void* ak_cache, int64_t num_slots, void* stream);
 
 /* Arguments of qkmla_decode (plain pointers and sizes). */
 typedef struct qkmla_decode_args {
@@ -134,7 +145,7 @@ typedef struct qkmla_decode_args {
     const float* q_rope;        /* [B][s_q][H][d_r] fp32, post-RoPE, not normalised */
     const float* gamma_rope_q;  /* [d_r] fp32 or NULL (ones) */
     const void* kv_cache;       /* [num_slots][d_c+d_r] cache_dtype */
-    const float* ak_cache;      /* [num_slots][G] fp32 */
+    const void* ak_cache;       /* [num_slots][G] fp32 (fp16 with QKMLA_FLAG_ALPHA_F16) */
     const int32_t* seq_lens;    /* [B] int32 device: tokens in the cache incl. this step's s_q */
     const int32_t* page_table;  /* [B][max_pages] int32 device, or NULL (contiguous) */
     int64_t num_slots;          /* slots in kv_cache / ak_cache (multiple of page_size) */

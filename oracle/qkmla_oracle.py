@@ -41,6 +41,10 @@ Readings where the pages are silent:
   * s_q > 1: query i of the step sees tokens t < seq_len - s_q + i + 1.
   * lse is the natural log of sum_t exp(l_t) with the logit scale included.
   * Plain-MLA mode (comparator): no norms, l = scale (q W^K_g^T . c^ + q_r . r^).
+  * Reduced-precision scalar cache (the scalar cache is the method's whole
+    storage overhead: Technical Summary, Key Contributions and Results): alpha^k
+    stored in IEEE half precision is the round-to-nearest-even fp16 of the fp32
+    alpha^k, and decode uses the stored value.
 """
 from __future__ import annotations
 
@@ -127,7 +131,8 @@ def absorb_query(q, gamma_q, gamma_k, w_k, eps: float, plain: bool = False):
     return qt, aq
 
 
-def append_tokens(c_new, r_new, w_k, gamma_rk, eps: float, cache_dtype: str, plain: bool = False):
+def append_tokens(c_new, r_new, w_k, gamma_rk, eps: float, cache_dtype: str, plain: bool = False,
+                  alpha_dtype: str = "f32"):
     """Cache entries of new tokens ([LAY], [DYN], [BLK]).
 
     c_new [N, d_c], r_new [N, d_r] (post-RoPE), w_k [G, d_c, d_h].
@@ -136,7 +141,8 @@ def append_tokens(c_new, r_new, w_k, gamma_rk, eps: float, cache_dtype: str, pla
       alpha^k = 1 / S(c^ W^K_g) for every group g,
       r^      = RoPE key normalised with its own statistic and gamma, then
                 rounded to the cache dtype.
-    Plain mode: r^ = rounded raw r, alpha^k = 1.
+    Plain mode: r^ = rounded raw r, alpha^k = 1.  alpha_dtype "f16": the
+    stored alpha^k is the fp16 rounding of its fp32 value ([DYN], [LAY]).
     """
     c_hat = cache_cast(c_new, cache_dtype)
     w = np.asarray(w_k, dtype=np.float64)
@@ -149,6 +155,11 @@ def append_tokens(c_new, r_new, w_k, gamma_rk, eps: float, cache_dtype: str, pla
     ak = np.empty((N, G))
     for g in range(G):
         ak[:, g] = inv_rms(c_hat @ w[g], eps)
+    if alpha_dtype == "f16":
+        # IEEE binary32 -> binary16, round to nearest even (numpy's cast)
+        ak = ak.astype(np.float32).astype(np.float16).astype(np.float64)
+    elif alpha_dtype != "f32":
+        raise ValueError(alpha_dtype)
     return c_hat, rope_key(r_new, gamma_rk, eps, cache_dtype), ak
 
 

@@ -16,7 +16,7 @@ def sequence_cache(w: W.Workload, b: int, plain: bool = False, host_seq=None):
     """(c^, r^, alpha^k) of sequence b in token order, fp64."""
     wk, _, _, _, grk = W.weights(w)
     c, r = W.sequence(w, b) if host_seq is None else host_seq
-    return O.append_tokens(c, r, wk, grk, w.eps, w.cache_dtype, plain=plain)
+    return O.append_tokens(c, r, wk, grk, w.eps, w.cache_dtype, plain=plain, alpha_dtype=w.alpha_dtype)
 
 
 def reference(w: W.Workload, seqs=None, plain: bool = False, heads=None, host_seqs=None):
@@ -46,3 +46,21 @@ def reference(w: W.Workload, seqs=None, plain: bool = False, heads=None, host_se
         o[:, :, hs] = og
         lse[:, :, hs] = lg
     return o, lse
+
+
+def reference_absorbed(w: W.Workload, seqs=None, plain: bool = False):
+    """Absorbed-form outputs for sequences `seqs` (default: all), from the
+    oracle's own cache state -- including alpha^k in the workload's A^k_cache
+    element type (fp16 rounding when alpha_dtype is "f16").
+
+    Returns (o [n, s_q, H, d_c], lse [n, s_q, H]).
+    """
+    seqs = list(range(w.B)) if seqs is None else list(seqs)
+    wk, gq, gk, grq, _ = W.weights(w)
+    q, qr = W.queries(w)
+    qs = q[seqs]
+    qt, aq = O.absorb_query(qs.reshape(-1, w.H, w.d_h), gq, gk, wk, w.eps, plain=plain)
+    qt = qt.reshape(len(seqs), w.s_q, w.H, w.d_c)
+    aq = aq.reshape(len(seqs), w.s_q, w.H)
+    caches = [sequence_cache(w, b, plain=plain) for b in seqs]
+    return O.decode_absorbed(qt, aq, qr[seqs], grq, caches, w.G, w.s_q, w.scale, w.eps, plain=plain)

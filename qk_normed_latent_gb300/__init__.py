@@ -23,6 +23,7 @@ F32, BF16 = 0, 1
 FLAG_PLAIN_MLA = 1
 FLAG_FORCE_SIMT = 2
 FLAG_TEST_STALL = 4
+FLAG_ALPHA_F16 = 8
 
 SYMBOLS = [
     "qkmla_absorb_query", "qkmla_append", "qkmla_decode_workspace_size", "qkmla_decode",
@@ -179,22 +180,34 @@ def absorb_query(q, gamma_q, gamma_k, w_k, eps: float, q_tilde, alpha_q, plain: 
     return q_tilde, alpha_q
 
 
+def _alpha_flag(ak_cache) -> int:
+    """QKMLA_FLAG_ALPHA_F16 for a float16 A^k_cache, 0 for fp32."""
+    torch = _torch()
+    if ak_cache is None or ak_cache.dtype == torch.float32:
+        return 0
+    if ak_cache.dtype == torch.float16:
+        return FLAG_ALPHA_F16
+    raise ValueError(f"qkmla: the A^k_cache is float32 or float16, not {ak_cache.dtype}")
+
+
 def prepare_append(c_new, k_rope_new, w_k, gamma_rope_k, slot_mapping, kv_cache, ak_cache, eps: float,
                    plain: bool = False) -> Prepared:
     """qkmla_append for fixed tensors (see append)."""
     N, d_c = c_new.shape
     d_r = k_rope_new.shape[1]
     G, _, d_h = w_k.shape
+    flags = (FLAG_PLAIN_MLA if plain else 0) | _alpha_flag(ak_cache)
     return Prepared("qkmla_append",
                     (_ptr(c_new), _ptr(k_rope_new), _ptr(w_k), _ptr(gamma_rope_k), _ptr(slot_mapping), N, G, d_c,
-                     d_h, d_r, float(eps), FLAG_PLAIN_MLA if plain else 0, _ptr(kv_cache),
+                     d_h, d_r, float(eps), flags, _ptr(kv_cache),
                      _dtype_code(kv_cache.dtype), _ptr(ak_cache), kv_cache.shape[0]))
 
 
 def append(c_new, k_rope_new, w_k, gamma_rope_k, slot_mapping, kv_cache, ak_cache, eps: float,
            plain: bool = False, stream=None):
     """Write new tokens (c_new [N, d_c], k_rope_new [N, d_r], fp32) into kv_cache
-    [num_slots, d_c+d_r] and ak_cache [num_slots, G] at slot_mapping [N] (int64)."""
+    [num_slots, d_c+d_r] and ak_cache [num_slots, G] (fp32, or float16 for the
+    reduced-precision scalar cache) at slot_mapping [N] (int64)."""
     prepare_append(c_new, k_rope_new, w_k, gamma_rope_k, slot_mapping, kv_cache, ak_cache, eps, plain)(stream)
 
 
@@ -214,7 +227,7 @@ def make_decode_args(q_tilde, alpha_q, q_rope, gamma_rope_q, kv_cache, ak_cache,
     a.B, a.s_q, a.H, a.G, a.d_c, a.d_r = B, s_q, H, int(G), d_c, d_r
     a.cache_dtype = _dtype_code(kv_cache.dtype)
     a.softmax_scale, a.eps = float(softmax_scale), float(eps)
-    a.flags = (FLAG_PLAIN_MLA if plain else 0) | (FLAG_FORCE_SIMT if force_simt else 0)
+    a.flags = (FLAG_PLAIN_MLA if plain else 0) | (FLAG_FORCE_SIMT if force_simt else 0) | _alpha_flag(ak_cache)
     a.num_splits = int(num_splits)
     a.o, a.o_dtype = _ptr(o), _dtype_code(o.dtype)
     a.lse = _ptr(lse)

@@ -83,7 +83,7 @@ template <typename CT, int S, int U>
 __global__ void __cluster_dims__(S, 1, 1) __launch_bounds__(kThreads)
 append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r_new, const float* __restrict__ wk,
                     const float* __restrict__ grk, const int64_t* __restrict__ slots, int N, int G, int d_r,
-                    float eps, int plain, CT* __restrict__ kv, float* __restrict__ ak, int64_t num_slots,
+                    float eps, int plain, CT* __restrict__ kv, void* __restrict__ ak, int ak_f16, int64_t num_slots,
                     int* status) {
     using namespace tc;
     constexpr int kDc = S * kKS, kDh = 16 * U;
@@ -175,7 +175,7 @@ append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r
             if (slot >= num_slots) {
                 report(status, QKMLA_ERR_DEVICE_BOUNDS);
             } else if (slot >= 0) {
-                ak[slot * G + g] = plain ? 1.f : 1.f / sqrtf(ss / (float)kDh + eps);
+                store_alpha(ak, slot * G + g, plain ? 1.f : 1.f / sqrtf(ss / (float)kDh + eps), ak_f16 != 0);
             }
         }
         // the RoPE key, normalised on its own: the token's 16 threads hold its d_r values
@@ -203,7 +203,7 @@ template <typename CT>
 __global__ void __launch_bounds__(kThreads)
 append_plain_kernel(const float* __restrict__ c_new, const float* __restrict__ r_new, const float* __restrict__ wk,
               const float* __restrict__ grk, const int64_t* __restrict__ slots, int N, int G, int d_c,
-              int d_h, int d_r, float eps, int plain, CT* __restrict__ kv, float* __restrict__ ak,
+              int d_h, int d_r, float eps, int plain, CT* __restrict__ kv, void* __restrict__ ak, int ak_f16,
               int64_t num_slots, int* status) {
     __shared__ float Cs[kTT][kKC + 1];
     extern __shared__ float Ws[];              // [kKC][d_h]
@@ -263,7 +263,7 @@ append_plain_kernel(const float* __restrict__ c_new, const float* __restrict__ r
             if (s >= num_slots) {
                 report(status, QKMLA_ERR_DEVICE_BOUNDS);
             } else if (s >= 0) {
-                ak[s * G + g] = plain ? 1.f : 1.f / sqrtf(ss / (float)d_h + eps);
+                store_alpha(ak, s * G + g, plain ? 1.f : 1.f / sqrtf(ss / (float)d_h + eps), ak_f16 != 0);
             }
         }
     }
@@ -281,30 +281,30 @@ append_plain_kernel(const float* __restrict__ c_new, const float* __restrict__ r
 
 template <typename CT, int S>
 cudaError_t launch_split(int U, const float* c_new, const float* r_new, const float* wk, const float* grk,
-                         const int64_t* slots, int N, int G, int d_r, float eps, bool plain, CT* kv, float* ak,
-                         int64_t num_slots, cudaStream_t s) {
+                         const int64_t* slots, int N, int G, int d_r, float eps, bool plain, CT* kv, void* ak,
+                         bool ak_f16, int64_t num_slots, cudaStream_t s) {
     auto k = U == 4 ? append_split_kernel<CT, S, 4> : append_split_kernel<CT, S, 8>;
     const int smem = split_smem_bytes(16 * U);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(((N + kFT - 1) / kFT) * S, G);
     return launch_pdl(k, grid, dim3(kThreads), smem, s, c_new, r_new, wk, grk, slots, N, G, d_r, eps, (int)plain, kv,
-                      ak, num_slots, device_status_ptr());
+                      ak, (int)ak_f16, num_slots, device_status_ptr());
 }
 
 template <typename CT>
 int launch_t(const float* c_new, const float* r_new, const float* wk, const float* grk, const int64_t* slots, int N,
-             int G, int d_c, int d_h, int d_r, float eps, bool plain, CT* kv, float* ak, int64_t num_slots,
-             cudaStream_t s) {
+             int G, int d_c, int d_h, int d_r, float eps, bool plain, CT* kv, void* ak, bool ak_f16,
+             int64_t num_slots, cudaStream_t s) {
     const int S = d_c / kKS;
     const bool split = d_c % kKS == 0 && (S == 2 || S == 4 || S == 8) && (d_h == 64 || d_h == 128) && d_r <= 64 &&
                        ((uintptr_t)c_new % 16) == 0 && ((uintptr_t)wk % 16) == 0;
     if (split) {
         const int U = d_h / 16;
         const cudaError_t e =
-            S == 2   ? launch_split<CT, 2>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, num_slots, s)
-            : S == 4 ? launch_split<CT, 4>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, num_slots, s)
-                     : launch_split<CT, 8>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, num_slots, s);
+            S == 2   ? launch_split<CT, 2>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, ak_f16, num_slots, s)
+            : S == 4 ? launch_split<CT, 4>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, ak_f16, num_slots, s)
+                     : launch_split<CT, 8>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, ak_f16, num_slots, s);
         if (e != cudaSuccess) return QKMLA_ERR_CUDA;
     } else {
         auto k = append_plain_kernel<CT>;
@@ -313,7 +313,7 @@ int launch_t(const float* c_new, const float* r_new, const float* wk, const floa
             return QKMLA_ERR_CUDA;
         dim3 grid((N + kTT - 1) / kTT, G);
         if (launch_pdl(k, grid, dim3(kThreads), smem, s, c_new, r_new, wk, grk, slots, N, G, d_c, d_h, d_r, eps,
-                       (int)plain, kv, ak, num_slots, device_status_ptr()) != cudaSuccess)
+                       (int)plain, kv, ak, (int)ak_f16, num_slots, device_status_ptr()) != cudaSuccess)
             return QKMLA_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
@@ -323,13 +323,13 @@ int launch_t(const float* c_new, const float* r_new, const float* wk, const floa
 
 int launch_append(const float* c_new, const float* r_new, const float* wk, const float* grk,
                   const int64_t* slots, int N, int G, int d_c, int d_h, int d_r, float eps, bool plain,
-                  void* kv, int cache_dtype, float* ak, int64_t num_slots, cudaStream_t s) {
+                  void* kv, int cache_dtype, void* ak, bool ak_f16, int64_t num_slots, cudaStream_t s) {
     if (N == 0) return QKMLA_OK;
     if (cache_dtype == QKMLA_F32)
         return launch_t<float>(c_new, r_new, wk, grk, slots, N, G, d_c, d_h, d_r, eps, plain, (float*)kv, ak,
-                               num_slots, s);
+                               ak_f16, num_slots, s);
     return launch_t<__nv_bfloat16>(c_new, r_new, wk, grk, slots, N, G, d_c, d_h, d_r, eps, plain,
-                                   (__nv_bfloat16*)kv, ak, num_slots, s);
+                                   (__nv_bfloat16*)kv, ak, ak_f16, num_slots, s);
 }
 
 }  // namespace qkmla

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "../../include/qkmla.h"
@@ -61,6 +62,17 @@ __device__ __forceinline__ int64_t slot_of(const int32_t* page_table, int b, int
     return page * page_size + (t % page_size);
 }
 
+// alpha^k entry `idx` of the A^k_cache, stored as fp32 or (f16) as its RNE half cast.
+__device__ __forceinline__ void store_alpha(void* ak, int64_t idx, float v, bool f16) {
+    if (f16) reinterpret_cast<__half*>(ak)[idx] = __float2half_rn(v);
+    else reinterpret_cast<float*>(ak)[idx] = v;
+}
+template <bool F16>
+__device__ __forceinline__ float load_alpha(const void* ak, int64_t idx) {
+    if constexpr (F16) return __half2float(reinterpret_cast<const __half*>(ak)[idx]);
+    else return reinterpret_cast<const float*>(ak)[idx];
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -93,7 +105,7 @@ int launch_absorb_tc(const float* q, const float* gq, const float* gk, const flo
                      int d_h, int d_c, float eps, bool plain, void* qt, int qt_dtype, float* aq, cudaStream_t s);
 int launch_append(const float* c_new, const float* r_new, const float* wk, const float* grk,
                   const int64_t* slots, int N, int G, int d_c, int d_h, int d_r, float eps, bool plain,
-                  void* kv, int cache_dtype, float* ak, int64_t num_slots, cudaStream_t s);
+                  void* kv, int cache_dtype, void* ak, bool ak_f16, int64_t num_slots, cudaStream_t s);
 
 struct DecodePlan {
     int kernel;            // 0 = simt, 1 = tcgen05

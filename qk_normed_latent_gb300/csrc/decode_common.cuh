@@ -32,7 +32,7 @@ struct TcParams {
     const float* aq;           // [B][s_q][H]
     const float* qr;           // [B][s_q][H][d_r]
     const float* grq;          // [d_r] or null
-    const float* ak;           // [num_slots][G]
+    const void* ak;            // [num_slots][G] fp32 or fp16 (the kernels' AKH template flag)
     const int32_t* seq_lens;
     const int32_t* page_table;
     int64_t num_pages;

@@ -83,12 +83,14 @@ static_assert(kBytesP <= 232448, "shared memory budget");
 // B) at 192, O (128 rows x 256 latents) at 256
 constexpr uint32_t kCSc = 0, kCSr = 64, kCP = 128, kCOwn = 192, kCO = 256;
 
-template <bool PLAIN>
+// AKH: A^k_cache entries are fp16 (else fp32)
+template <bool PLAIN, bool AKH>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsP, 1)
 decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
                    const __grid_constant__ CUtensorMap tm_q, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smraw[];
-    uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned base, formed from smraw itself so accesses stay in the shared window
+    uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     uint8_t* sQ = sm + kOffQ;
     uint8_t* sX = sm + kOffX;
     uint8_t* sY = sm + kOffY;
@@ -206,7 +208,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             }
             return (int)(page * p.page_size + (t0 % p.page_size));
         };
-        const uint32_t tx = (uint32_t)(kSLat + kSRope) + (PLAIN ? 0u : (uint32_t)(kT * p.G * 4));
+        const uint32_t ak_bytes = PLAIN ? 0u : (uint32_t)(kT * p.G * (AKH ? 2 : 4));
+        const uint32_t tx = (uint32_t)(kSLat + kSRope) + ak_bytes;
         int slot_batch = slot_of_tile(lane);
         for (int j = 0; j < n_t; ++j) {
             if ((j & 31) == 0 && j > 0) slot_batch = slot_of_tile(j + lane);
@@ -227,8 +230,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                         tma_load_2d(stg + blk * (kT * 128), &tm_lat, rank * kHalfLat + blk * 64, slot0, &full[s]);
                     tma_load_2d(stg + kSLat, &tm_rope, kDC + rank * kHalfRope, slot0, &full[s]);
                     if (!PLAIN)
-                        bulk_load(stg + kSLat + kSRope, p.ak + (int64_t)slot0 * p.G, (uint32_t)(kT * p.G * 4),
-                                  &full[s]);
+                        bulk_load(stg + kSLat + kSRope, (const uint8_t*)p.ak + (int64_t)slot0 * p.G * (AKH ? 2 : 4),
+                                  ak_bytes, &full[s]);
                 }
             }
             if (!__shfl_sync(0xffffffffu, go, 0)) break;
@@ -339,7 +342,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 const int valid = min(kT, L - (jt0 + j) * kT);
                 const bool got_s = __all_sync(0xffffffffu, wait_bounded(sfull, j & 1, p.status));
                 tc_fence_after();
-                const float* ak_t = (const float*)(sm + kOffStage + s * kStageB + kSLat + kSRope);
+                const void* ak_t = sm + kOffStage + s * kStageB + kSLat + kSRope;
 #pragma unroll
                 for (int c = 0; c < kT / 16; ++c) {
                     uint32_t sc[16], sr[16];
@@ -350,7 +353,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                     for (int jj = 0; jj < 16; ++jj) {
                         const int t = 16 * c + jj;
                         pv[t] = PLAIN ? rs * __uint_as_float(sc[jj])
-                                      : fmaf(coef * ak_t[t * p.G + g], __uint_as_float(sc[jj]), __uint_as_float(sr[jj]));
+                                      : fmaf(coef * load_alpha<AKH>(ak_t, t * p.G + g), __uint_as_float(sc[jj]),
+                                             __uint_as_float(sr[jj]));
                     }
                 }
                 tc_fence_before();
@@ -613,7 +617,8 @@ int launch_pair(const qkmla_decode_args* a, const TcParams& tp, int max_items, c
     if (!make_map(&qmap, a->q_tilde, (int64_t)a->B * a->s_q * a->H, kDC, 64, kR, CU_TENSOR_MAP_SWIZZLE_128B))
         return QKMLA_ERR_CUDA;
     const bool plain = (a->flags & QKMLA_FLAG_PLAIN_MLA) != 0;
-    auto k = plain ? decode_pair_kernel<true> : decode_pair_kernel<false>;
+    const bool akh = !plain && (a->flags & QKMLA_FLAG_ALPHA_F16) != 0;
+    auto k = plain ? decode_pair_kernel<true, false> : akh ? decode_pair_kernel<false, true> : decode_pair_kernel<false, false>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytesP) != cudaSuccess)
         return QKMLA_ERR_CUDA;
     dim3 grid(2 * a->s_q, max_items);

@@ -27,7 +27,7 @@ struct SimtParams {
     const float* qr;
     const float* grq;
     const void* kv;
-    const float* ak;
+    const void* ak;     // fp32, or fp16 when ak_f16
     const int32_t* seq_lens;
     const int32_t* page_table;
     int64_t num_pages;
@@ -35,6 +35,7 @@ struct SimtParams {
     int B, s_q, H, G, d_c, d_r;
     float scale, eps;
     int plain;
+    int ak_f16;
     int nsplit;
     float* o_part;      // [rows*H][nsplit][d_c] when nsplit > 1
     float* lse_part;    // [rows*H][nsplit]
@@ -125,7 +126,9 @@ decode_simt_kernel(SimtParams p) {
         }
         if (tid < kTC) {
             const int64_t s = slot[tid];
-            aks[tid] = (s >= 0) ? (p.plain ? 1.f : p.ak[s * p.G + g]) : 0.f;
+            aks[tid] = (s >= 0) ? (p.plain ? 1.f
+                                           : p.ak_f16 ? load_alpha<true>(p.ak, s * p.G + g) : load_alpha<false>(p.ak, s * p.G + g))
+                                : 0.f;
         }
         __syncthreads();
         // logits (log2 domain)
@@ -262,6 +265,7 @@ int launch_decode_simt(const qkmla_decode_args* a, const DecodePlan& plan, cudaS
     p.scale = a->softmax_scale;
     p.eps = a->eps;
     p.plain = (a->flags & QKMLA_FLAG_PLAIN_MLA) ? 1 : 0;
+    p.ak_f16 = (!p.plain && (a->flags & QKMLA_FLAG_ALPHA_F16)) ? 1 : 0;
     p.nsplit = plan.num_splits;
     const int64_t rows_h = (int64_t)a->B * a->s_q * a->H;
     p.o_part = (float*)a->workspace;

@@ -97,7 +97,8 @@ __device__ __forceinline__ uint32_t pt_offset(int r, int t, int rows_o) {
     return (uint32_t)(t >> 6) * (uint32_t)(rows_o * 128) + sw128_offset(r, t & 63);
 }
 
-template <int DC, int DR, bool PLAIN, int NST, int KT>
+// AKH: A^k_cache entries are fp16 (else fp32)
+template <int DC, int DR, bool PLAIN, int NST, int KT, bool AKH>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
                  const __grid_constant__ CUtensorMap tm_q, const TcParams p) {
@@ -183,7 +184,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
         }
         return page * p.page_size + (t0 % p.page_size);
     };
-    const uint32_t ak_bytes = PLAIN ? 0u : (uint32_t)(KT * p.G * 4);
+    const uint32_t ak_bytes = PLAIN ? 0u : (uint32_t)(KT * p.G * (AKH ? 2 : 4));
     auto issue_tile = [&](int j, int64_t slot0) {        // lane 0 of warp 0
         const int s = j % NST;
         uint8_t* stg = sm + LY::kOffStage + s * LY::kStage;
@@ -195,7 +196,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             tma_load_2d(stg + LY::kSLat, &tm_lat, DC, (int)slot0, &full[s]);
         else
             tma_load_2d(stg + LY::kSLat, &tm_rope, DC, (int)slot0, &full[s]);
-        if (!PLAIN) bulk_load(stg + LY::kSLat + LY::kSRope, p.ak + slot0 * p.G, ak_bytes, &full[s]);
+        if (!PLAIN)
+            bulk_load(stg + LY::kSLat + LY::kSRope, (const uint8_t*)p.ak + slot0 * p.G * (AKH ? 2 : 4), ak_bytes, &full[s]);
     };
     int64_t slot_batch = 0;
 
@@ -380,7 +382,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             if (!got_s) *(volatile int*)abort_flag = 1;
             tc_fence_after();
             uint8_t* stg = sm + LY::kOffStage + s * LY::kStage;
-            const float* ak_t = (const float*)(stg + LY::kSLat + LY::kSRope);
+            const void* ak_t = stg + LY::kSLat + LY::kSRope;
             const int valid = min(KT, L - tile * KT);
             float lg[kQ4][16];
 #pragma unroll
@@ -395,7 +397,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                     if (PLAIN)
                         lg[q][jj] = rs * __uint_as_float(sc[jj]);
                     else
-                        lg[q][jj] = fmaf(coef * ak_t[t * p.G + g], __uint_as_float(sc[jj]), __uint_as_float(sr[jj]));
+                        lg[q][jj] = fmaf(coef * load_alpha<AKH>(ak_t, t * p.G + g), __uint_as_float(sc[jj]),
+                                         __uint_as_float(sr[jj]));
                     if (t >= valid) lg[q][jj] = -INFINITY;
                 }
             }
@@ -759,12 +762,12 @@ combine_var_kernel(const float* __restrict__ o_part, const float* __restrict__ l
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-template <int DC, int DR, bool PLAIN, int NST>
+template <int DC, int DR, bool PLAIN, int NST, bool AKH>
 int launch_kernel(const CUtensorMap& lat, const CUtensorMap& rope, const CUtensorMap& qmap, const TcParams& tp,
                   int n_rb, int max_items, cudaStream_t s) {
     constexpr int KT = tile_of<DC>();
     using LY = Layout<DC, DR, NST, KT>;
-    auto k = decode_tc_kernel<DC, DR, PLAIN, NST, KT>;
+    auto k = decode_tc_kernel<DC, DR, PLAIN, NST, KT, AKH>;
     static_assert(LY::kBytes <= 232448, "shared memory budget");
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes) != cudaSuccess)
         return QKMLA_ERR_CUDA;
@@ -923,15 +926,18 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     tp.wait_ns = stall ? 1000000ull : kWaitNs;
     tp.withhold_tile = stall ? 1 : -1;
     const bool plain = (a->flags & QKMLA_FLAG_PLAIN_MLA) != 0;
+    const bool akh = !plain && (a->flags & QKMLA_FLAG_ALPHA_F16) != 0;
     int rc;
     if (pair_shape(a)) {
         rc = launch_pair(a, tp, max_items, s);
     } else if (a->d_c == 512) {
-        rc = plain ? launch_kernel<512, 64, true, 4>(lat, rope, qmap, tp, n_rb, max_items, s)
-                   : launch_kernel<512, 64, false, 4>(lat, rope, qmap, tp, n_rb, max_items, s);
+        rc = plain ? launch_kernel<512, 64, true, 4, false>(lat, rope, qmap, tp, n_rb, max_items, s)
+             : akh ? launch_kernel<512, 64, false, 4, true>(lat, rope, qmap, tp, n_rb, max_items, s)
+                   : launch_kernel<512, 64, false, 4, false>(lat, rope, qmap, tp, n_rb, max_items, s);
     } else {
-        rc = plain ? launch_kernel<256, 32, true, 4>(lat, rope, qmap, tp, n_rb, max_items, s)
-                   : launch_kernel<256, 32, false, 4>(lat, rope, qmap, tp, n_rb, max_items, s);
+        rc = plain ? launch_kernel<256, 32, true, 4, false>(lat, rope, qmap, tp, n_rb, max_items, s)
+             : akh ? launch_kernel<256, 32, false, 4, true>(lat, rope, qmap, tp, n_rb, max_items, s)
+                   : launch_kernel<256, 32, false, 4, false>(lat, rope, qmap, tp, n_rb, max_items, s);
     }
     if (rc != QKMLA_OK) return rc;
     const int combine_ctas = std::min(a->B * a->s_q * a->H, 2 * sms);

@@ -14,10 +14,11 @@ import workloads as W
 from . import (F32, BF16, append, decode_workspace_size, decode_raw, make_decode_args, prepare_absorb_query,
                prepare_append)
 
-_TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+_TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 # quiet-NaN bit patterns written into untouched cache slots
 SENTINEL_BF16 = 0x7FC1
 SENTINEL_F32 = 0x7FC00001
+SENTINEL_F16 = 0x7E01
 
 
 def packed(parts, device, empty=False):
@@ -50,6 +51,8 @@ def packed(parts, device, empty=False):
 def sentinel_fill(t: torch.Tensor) -> None:
     if t.dtype == torch.bfloat16:
         t.view(torch.int16).fill_(SENTINEL_BF16)
+    elif t.dtype == torch.float16:
+        t.view(torch.int16).fill_(SENTINEL_F16)
     elif t.dtype == torch.float32:
         t.view(torch.int32).fill_(SENTINEL_F32)
     else:
@@ -78,7 +81,7 @@ class DeviceState:
         self.grk = torch.from_numpy(grk).to(d)
         cdt = _TORCH_DT[w.cache_dtype]
         self.kv = torch.empty((self.num_slots, w.d_c + w.d_r), dtype=cdt, device=d)
-        self.ak = torch.empty((self.num_slots, w.G), dtype=torch.float32, device=d)
+        self.ak = torch.empty((self.num_slots, w.G), dtype=_TORCH_DT[w.alpha_dtype], device=d)
         if sentinel:
             sentinel_fill(self.kv)
             sentinel_fill(self.ak)

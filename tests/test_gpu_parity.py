@@ -456,3 +456,86 @@ def test_graph_replay_matches_direct_calls(Q, widx):
     torch.cuda.synchronize()
     assert_status_ok(Q)
     assert torch.equal(st.o, o1) and torch.equal(st.lse, l1)
+
+
+# ---------------------------------------------------------------------------
+# reduced-precision scalar cache: A^k_cache in fp16
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("widx", [1, 2])
+def test_append_f16_alpha_is_the_rne_cast_of_the_fp32_alpha(Q, widx):
+    """The fp16 A^k_cache holds the round-to-nearest-even cast of the fp32 alpha^k
+    the same kernel writes to an fp32 cache (bit for bit); the latent and RoPE key
+    rows do not change; untouched slots keep their sentinel bits."""
+    from qk_normed_latent_gb300.pipeline import sentinel_fill
+    w = W.WORKLOADS[widx]
+    wk, _, _, _, grk = W.weights(w)
+    c, r = W.sequence(W.small(w, 1, (203,)), 0)
+    num_slots = 512
+    slots = np.random.default_rng(8).choice(num_slots, size=203, replace=False).astype(np.int64)
+    d = "cuda"
+    outs = []
+    for adt in (torch.float32, torch.float16):
+        kv = torch.empty((num_slots, w.d_c + w.d_r), dtype=torch.bfloat16, device=d)
+        ak = torch.empty((num_slots, w.G), dtype=adt, device=d)
+        sentinel_fill(kv)
+        sentinel_fill(ak)
+        ak0 = ak.clone()
+        Q.append(torch.from_numpy(c).to(d), torch.from_numpy(r).to(d), torch.from_numpy(wk).to(d),
+                 torch.from_numpy(grk).to(d), torch.from_numpy(slots).to(d), kv, ak, w.eps)
+        assert_status_ok(Q)
+        outs.append((kv.cpu(), ak.cpu(), ak0.cpu()))
+    (kv32, ak32, _), (kv16, ak16, ak16_0) = outs
+    assert torch.equal(kv32.view(torch.int16), kv16.view(torch.int16))
+    sl = torch.from_numpy(slots)
+    assert torch.equal(ak16[sl].view(torch.int16), ak32[sl].to(torch.float16).view(torch.int16))
+    untouched = torch.from_numpy(np.setdiff1d(np.arange(num_slots), slots))
+    assert torch.equal(ak16[untouched].view(torch.int16), ak16_0[untouched].view(torch.int16))
+    # and the oracle's fp16 alpha^k: within one fp16 rounding of the fp32 difference
+    _, _, a_ref = O.append_tokens(c, r, wk, grk, w.eps, "bf16", alpha_dtype="f16")
+    got = ak16[sl].float().numpy().astype(np.float64)
+    assert np.all(np.abs(got - a_ref) <= 2.0 ** -10 * np.abs(a_ref))
+
+
+ALPHA_CASES = {
+    # CUDA cores (fp32 latent cache), 64-row tensor-core kernel (d_c = 256 and 512), CTA-pair kernel
+    "tiny_fp32_af16": (0, dict(B=1, lens=(256,))),
+    "small_af16": (1, dict(B=3, lens=(1024, 1500, 8192))),
+    "dsv3_H64_af16": (2, dict(B=3, lens=(1000, 4096, 700), kw=dict(H=64, G=4))),
+    "dsv3_af16": (2, dict(B=4, lens=(4096, 1000, 640, 3000))),
+    "mixed_sq2_af16": (4, dict(B=3, lens=(600, 5000, 20000))),
+}
+
+
+@pytest.mark.parametrize("name", list(ALPHA_CASES))
+def test_decode_f16_alpha_matches_oracle(Q, name):
+    """fp16 alpha^k against the explicit definition (the cache dtype's tolerance)
+    and against the absorbed form evaluated on the oracle's own fp16 scalar cache
+    (fp32 latent cache: 1e-5, as the fp32 path; bf16: the bf16 tolerance)."""
+    from qk_normed_latent_gb300.pipeline import DeviceState
+    widx, red = ALPHA_CASES[name]
+    w = W.small(W.WORKLOADS[widx], red["B"], red["lens"], alpha_dtype="f16", **red.get("kw", {}))
+    st = DeviceState(w)
+    assert st.ak.dtype == torch.float16
+    st.step()
+    assert_status_ok(Q)
+    o_ref, lse_ref = OR.reference(w)
+    kind_explicit = "bf16"        # fp16 alpha^k is a 2^-11 approximation of the explicit statistic
+    check_close(_np(st.o), o_ref, kind_explicit, f"{name} o vs explicit")
+    check_close(_np(st.lse), lse_ref, kind_explicit, f"{name} lse vs explicit")
+    # the fp16 code of each alpha^k is decided from the kernel's fp32 value and from
+    # the oracle's (fp64 -> fp32); they can fall on either side of a rounding tie,
+    # so a code may differ by one fp16 step -- any other difference is an error
+    lens = W.seq_lens(w)
+    ps_, mp_, _, table = W.page_layout(w, lens)
+    ak_gpu = st.ak.float().cpu().numpy().astype(np.float64)
+    ties = 0
+    for b in range(w.B):
+        a_ref = OR.sequence_cache(w, b)[2]
+        a_got = ak_gpu[W.slots_of(table, ps_, b, np.arange(int(lens[b])))]
+        diff = a_got != a_ref
+        ties += int(diff.sum())
+        assert np.all(np.abs(a_got[diff] - a_ref[diff]) <= 2.0 ** -10 * np.abs(a_ref[diff]))
+    o_abs, lse_abs = OR.reference_absorbed(w)
+    kind_abs = w.cache_dtype if ties == 0 else "bf16"
+    check_close(_np(st.o), o_abs, kind_abs, f"{name} o vs absorbed f16-alpha ({ties} tie codes)")
+    check_close(_np(st.lse), lse_abs, kind_abs, f"{name} lse vs absorbed f16-alpha ({ties} tie codes)")

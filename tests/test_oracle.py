@@ -461,3 +461,59 @@ def test_mutation_rope_key_is_caught(monkeypatch, cache, mutation):
     assert gap() < 1e-11
     monkeypatch.setattr(O.qkmla_oracle, "rope_key", bad)
     assert gap() > 1e-5
+
+
+# --------------------------------------------------------------------------
+# reduced-precision scalar cache: alpha^k stored in fp16
+# --------------------------------------------------------------------------
+def test_f16_alpha_is_the_rne_cast_of_fp32_alpha():
+    case = _rand_case(70, B=1, lens=(90,))
+    c, r = case["seqs_raw"][0]
+    _, _, a32 = O.append_tokens(c, r, case["wk"], case["grk"], case["eps"], "bf16")
+    _, _, a16 = O.append_tokens(c, r, case["wk"], case["grk"], case["eps"], "bf16", alpha_dtype="f16")
+    ref = torch.from_numpy(a32.astype(np.float32)).to(torch.float16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(a16, ref)
+    # fp16 keeps 11 significant bits: one RNE rounding moves a value by at most 2^-11 of it
+    assert np.max(np.abs(a16 / a32 - 1)) <= 2.0 ** -11 + 1e-7
+
+
+def test_f16_alpha_is_exact_when_alpha_is_a_power_of_two():
+    """With W^K = I, eps = 0 and latents of constant magnitude 2^m per token,
+    alpha^k = 2^-m is exact in fp16: the half-precision scalar cache changes nothing."""
+    g = np.random.default_rng(71)
+    d = 16
+    wk = np.eye(d, dtype=np.float32)[None]                         # G = 1, d_c = d_h = 16
+    L = 40
+    c = np.sign(g.standard_normal((L, d))).astype(np.float32) * (2.0 ** g.integers(-3, 4, size=(L, 1))).astype(np.float32)
+    r = g.standard_normal((L, 8)).astype(np.float32)
+    q = g.standard_normal((1, 1, 4, d)).astype(np.float32)
+    qr = g.standard_normal((1, 1, 4, 8)).astype(np.float32)
+    gq = np.ones(d, np.float32)
+    gk = np.ones(d, np.float32)
+    outs = []
+    for ad in ("f32", "f16"):
+        ch, rh, ak = O.append_tokens(c, r, wk, None, 0.0, "f32", alpha_dtype=ad)
+        qt, aq = O.absorb_query(q[:, 0], gq, gk, wk, 0.0)
+        outs.append(O.decode_absorbed(qt[:, None], aq[:, None], qr, None, [(ch, rh, ak)], 1, 1, 0.25, 0.0))
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])
+
+
+def test_f16_alpha_moves_logits_within_the_rounding_bound():
+    """Each content logit moves by at most |content logit| 2^-11 (one fp16 RNE
+    rounding of alpha^k), so lse moves by at most the largest such change."""
+    case = _rand_case(72, B=1, lens=(300,), H=8, G=2)
+    c, r = case["seqs_raw"][0]
+    qt, aq = O.absorb_query(case["q"][:, 0], case["gq"], case["gk"], case["wk"], case["eps"])
+    res, cont = [], None
+    for ad in ("f32", "f16"):
+        ch, rh, ak = O.append_tokens(c, r, case["wk"], case["grk"], case["eps"], "f32", alpha_dtype=ad)
+        res.append(O.decode_absorbed(qt[:, None], aq[:, None], case["qr"], case["grq"], [(ch, rh, ak)], case["G"], 1,
+                                     case["scale"], case["eps"]))
+        if ad == "f32":
+            g_of = O.group_of_head(case["H"], case["G"])
+            cont = case["scale"] * np.abs(aq[0][None, :] * ak[:, g_of] * (ch @ qt[0].T))    # [L, H]
+    bound = cont.max(axis=0) * 2.0 ** -11 * 1.001
+    dl = np.abs(res[1][1][0, 0] - res[0][1][0, 0])
+    assert np.all(dl <= bound + 1e-12)
+    assert np.any(dl > 0)                                  # the rounding is visible

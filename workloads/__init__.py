@@ -51,6 +51,7 @@ class Workload:
     seed: int
     eps: float = 1e-6
     rope_gamma_std: float = 0.0   # RoPE gammas = 1 + std * N(0,1) (0: ones, the pages name none)
+    alpha_dtype: str = "f32"      # A^k_cache element type: "f32" or "f16"
 
     @property
     def scale(self) -> float:
