@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", type=int, default=4,
                     help="index into workloads.WORKLOADS (default 4: B=128, s_q=2, the largest single-GPU workload)")
+    ap.add_argument("--s-q", type=int, default=0,
+                    help="query tokens per sequence in a step (multi-token prediction / chunked prefill); "
+                         "0 keeps the workload's own")
     ap.add_argument("--batch", type=int, default=0,
                     help="keep only the first N sequences of the workload (a reduced case for profiling)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -254,6 +257,8 @@ def main():
     w0 = W.WORKLOADS[args.workload]
     if 0 < args.batch < w0.B:
         w0 = W.small(w0, args.batch, W.seq_lens(w0)[:args.batch], name=f"{w0.name}_first{args.batch}")
+    if args.s_q > 0 and args.s_q != w0.s_q:
+        w0 = w0.with_(s_q=args.s_q, n_append=args.s_q, name=f"{w0.name}_sq{args.s_q}")
 
     if args.impl == "reference":
         if rank != 0:
@@ -418,6 +423,22 @@ def main():
             raise RuntimeError("device status error in the comparator timing")
         del sp_step_g, sp_dec_g, sp, sb_step_g, sb_dec_g, sb
 
+    # the value up-projection of this step's latent output (its own call, timed alone)
+    wv = torch.from_numpy(W.value_weights(w)).to("cuda").to(torch.bfloat16)
+    v_out = torch.empty((w.B, w.s_q, w.H, wv.shape[2]), dtype=torch.float32, device="cuda")
+    up_call = Q.prepare_up_project(st.o, wv, v_out)
+    up_g = capture(lambda: up_call())
+    up_ms = statistics.median(timed(up_g, min(args.steps, 100)))
+    if Q.get_device_status() != 0:
+        raise RuntimeError("device status error in the up-projection timing")
+    up_rows = w.B * w.s_q * w.H
+    up_bytes = up_rows * w.d_c * 4 + wv.numel() * 2 + up_rows * wv.shape[2] * 4
+    up_flops = 2 * up_rows * w.d_c * wv.shape[2]
+    up_project = {"ms": up_ms, "gbs": up_bytes / (up_ms * 1e-3) / 1e9, "tflops": up_flops / (up_ms * 1e-3) / 1e12,
+                  "bound": "hbm", "frac_of_hbm": up_bytes / (up_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                  "algorithmic_bytes": up_bytes, "algorithmic_flops": up_flops}
+    del up_g
+
     # end to end through the public API with host buffers: H2D of the step's inputs,
     # the three calls, D2H of o and lse, all inside the timed region.  The inputs
     # (q, q_rope and the step's new tokens) live in one pinned host buffer and one
@@ -463,6 +484,7 @@ def main():
             "roofline": roof,
             "plain_mla": plain,
             "alpha_f16": alpha_f16,
+            "up_project": up_project,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,

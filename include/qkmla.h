@@ -242,6 +242,29 @@ int qkmla_decode_launch_count(const qkmla_decode_args* a);
  */
 int qkmla_decode_noalloc(const qkmla_decode_args* a, void* stream);
 
+/*
+ * qkmla_up_project -- per-head values from the latent-space decode output.
+ * Source: Technical Summary, Problem Statement (MLA keeps the low-dimensional
+ * latent and recovers per-head quantities through up-projections, as W^K_g
+ * recovers the key); the abstract (decode keeps the latent path, so attention
+ * returns o = sum_t p_t c_t).  The value of head h is recovered once per query
+ * row instead of once per cached token:
+ *
+ *   out[r][h][j] = sum_n o[r][h][n] * W^V[g(h)][n][j],   g(h) = h / (H / G_v)
+ *
+ * which equals softmax attention over materialised values c_t W^V_{g(h)}
+ * (the softmax weights sum to one).
+ * o     [rows][H][d_c] in o_dtype (QKMLA_F32 or QKMLA_BF16): qkmla_decode's output
+ * w_v   [G_v][d_c][d_v] bf16 (G_v = H: one matrix per head)
+ * out   [rows][H][d_v] in out_dtype (QKMLA_F32 or QKMLA_BF16)
+ * Tensor cores, fp32 accumulation; an fp32 o is split into two bf16 parts
+ * (fp32-level accuracy).  Errors: INVALID for null pointers, non-positive
+ * sizes, H % G_v != 0 or a base not 16-byte aligned; UNSUPPORTED for other
+ * dtypes, d_c % 64 != 0, or d_v not in {64, 128, 192, 256}.
+ */
+int qkmla_up_project(const void* o, int o_dtype, const void* w_v, int rows, int H, int G_v, int d_c,
+                     int d_v, void* out, int out_dtype, void* stream);
+
 /* Bytes of scratch qkmla_decode_noalloc can use (its fixed array). */
 size_t qkmla_decode_noalloc_max_workspace(void);
 

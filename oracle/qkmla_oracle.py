@@ -27,6 +27,8 @@ full key caching", arXiv 2606.16310):
   [EXACT] thelatestinai.com abstract: the absorbed form is exactly equivalent
          to explicit post-projection QK RMSNorm in exact arithmetic and keeps
          MLA's latent decode path.
+  [UP]   Technical Summary, "Problem Statement": MLA keeps the latent and
+         recovers per-head quantities through up-projections (W^K_g for keys).
 
 Readings where the pages are silent:
   * g(h) = h // (H/G) (contiguous head groups).
@@ -37,7 +39,9 @@ Readings where the pages are silent:
     normalised with its own gamma (ones by default) and stored normalised;
     the query RoPE part is normalised per head inside decode.
   * alpha^k is computed from the stored (cache-dtype-rounded) latent.
-  * Values are the latents: o = sum_t p_t c^_t (latent-space output).
+  * Values are the latents: o = sum_t p_t c^_t (latent-space output).  Per-head
+    values come from o by a value up-projection W^V_{g(h)} (per group, like
+    W^K_g; G_v = H is one matrix per head), stored in bf16.
   * s_q > 1: query i of the step sees tokens t < seq_len - s_q + i + 1.
   * lse is the natural log of sum_t exp(l_t) with the logit scale included.
   * Plain-MLA mode (comparator): no norms, l = scale (q W^K_g^T . c^ + q_r . r^).
@@ -54,7 +58,7 @@ __all__ = [
     "bf16_rne", "cache_cast", "inv_rms", "group_of_head",
     "absorb_query", "append_tokens", "rope_key", "full_keys",
     "decode_explicit", "decode_absorbed", "combine_partials",
-    "valid_length", "cache_write", "cache_gather",
+    "valid_length", "cache_write", "cache_gather", "up_project",
 ]
 
 
@@ -303,6 +307,19 @@ def combine_partials(o_parts, lse_parts):
     lse = m + np.log(s)
     o = np.einsum("s...,s...d->...d", w / s, o_parts)
     return o, lse
+
+
+def up_project(o, w_v):
+    """Per-head values from the latent output ([UP]): out[..., h, :] = o[..., h, :] W^V_{g(h)}.
+    o [..., H, d_c], w_v [G_v, d_c, d_v] (the stored weights).  Returns [..., H, d_v]."""
+    o = np.asarray(o, np.float64)
+    w = np.asarray(w_v, np.float64)
+    H = o.shape[-2]
+    g_of = group_of_head(H, w.shape[0])
+    out = np.empty(o.shape[:-1] + (w.shape[2],))
+    for h in range(H):
+        out[..., h, :] = o[..., h, :] @ w[g_of[h]]
+    return out
 
 
 # ----------------------------------------------------------------------------

@@ -28,7 +28,7 @@ FLAG_ALPHA_F16 = 8
 SYMBOLS = [
     "qkmla_absorb_query", "qkmla_append", "qkmla_decode_workspace_size", "qkmla_decode",
     "qkmla_get_device_status", "qkmla_status_string", "qkmla_version", "qkmla_decode_kernel_name",
-    "qkmla_decode_launch_count",
+    "qkmla_decode_launch_count", "qkmla_up_project",
 ]
 
 
@@ -100,6 +100,8 @@ def lib() -> ctypes.CDLL:
         L.qkmla_decode_kernel_name.restype = ctypes.c_char_p
         L.qkmla_decode_launch_count.argtypes = [ctypes.POINTER(DecodeArgs)]
         L.qkmla_decode_launch_count.restype = i
+        L.qkmla_up_project.argtypes = [vp, i, vp, i, i, i, i, i, vp, i, vp]
+        L.qkmla_up_project.restype = i
         if hasattr(L, "qkmla_decode_noalloc"):
             L.qkmla_decode_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), vp]
             L.qkmla_decode_noalloc.restype = i
@@ -266,6 +268,21 @@ def decode(q_tilde, alpha_q, q_rope, gamma_rope_q, kv_cache, ak_cache, seq_lens,
         a.workspace, a.workspace_bytes = workspace.data_ptr(), need
     decode_raw(a, stream)
     return o, lse
+
+
+def prepare_up_project(o, w_v, out) -> Prepared:
+    """qkmla_up_project for fixed tensors (see up_project)."""
+    H, d_c = o.shape[-2], o.shape[-1]
+    rows = o.numel() // (H * d_c)
+    G_v, _, d_v = w_v.shape
+    return Prepared("qkmla_up_project", (_ptr(o), _dtype_code(o.dtype), _ptr(w_v), rows, H, G_v, d_c, d_v, _ptr(out),
+                                         _dtype_code(out.dtype)))
+
+
+def up_project(o, w_v, out, stream=None):
+    """out [..., H, d_v] = o [..., H, d_c] @ W^V[g(h)] with w_v [G_v, d_c, d_v] (bf16)."""
+    prepare_up_project(o, w_v, out)(stream)
+    return out
 
 
 def get_device_status(stream=None) -> int:

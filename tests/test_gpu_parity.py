@@ -242,8 +242,18 @@ CASES = {
     "dsv3_H64_grope": (2, dict(B=3, lens=(1000, 4096, 700), kw=dict(H=64, G=4, rope_gamma_std=0.1))),
     "dsv3_grope": (2, dict(B=4, lens=(4096, 1000, 640, 3000), kw=dict(rope_gamma_std=0.1))),
     "mixed_sq2_grope": (4, dict(B=3, lens=(600, 5000, 20000), kw=dict(rope_gamma_std=0.1))),
+    # more query tokens per step (multi-token prediction, chunked prefill), causal within the step:
+    # CTA-pair kernel, 64-row kernel and CUDA cores
+    "dsv3_sq4": (4, dict(B=3, lens=(4, 700, 9000), kw=dict(s_q=4, n_append=4))),
+    "dsv3_sq16": (4, dict(B=2, lens=(16, 3001), kw=dict(s_q=16, n_append=16))),
+    "dsv3_sq16_clean": (4, dict(B=2, lens=(16, 3001), kw=dict(s_q=16, n_append=16, outlier_frac=0.0))),
+    "small_sq8": (1, dict(B=3, lens=(8, 1000, 4100), kw=dict(s_q=8, n_append=8))),
+    "tiny_fp32_sq8": (0, dict(B=2, lens=(9, 256), kw=dict(s_q=8, n_append=8))),
 }
-EDGE = {"dsv3_ragged", "mixed_sq2_ragged", "small_ragged", "small_B160_sched", "dsv3_B136_sched"}
+# sequences of 1-130 tokens (the larger-s_q cases include one of exactly s_q tokens, so its first
+# query token sees one token)
+EDGE = {"dsv3_ragged", "mixed_sq2_ragged", "small_ragged", "small_B160_sched", "dsv3_B136_sched",
+        "dsv3_sq4", "dsv3_sq16", "small_sq8"}
 
 
 def make_args_only(Q, w):

@@ -517,3 +517,49 @@ def test_f16_alpha_moves_logits_within_the_rounding_bound():
     dl = np.abs(res[1][1][0, 0] - res[0][1][0, 0])
     assert np.all(dl <= bound + 1e-12)
     assert np.any(dl > 0)                                  # the rounding is visible
+
+
+# --------------------------------------------------------------------------
+# value up-projection
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("G_v", [2, 8])
+def test_up_projection_equals_attention_over_materialised_values(G_v):
+    """o W^V (the latent path, projected once per row) equals torch attention with
+    every value v_t = c^_t W^V_{g(h)} materialised (softmax weights sum to one)."""
+    case = _rand_case(80, B=2, s_q=2, H=8, G=2, lens=(45, 70), cache="bf16")
+    g = np.random.default_rng(81)
+    wv = O.bf16_rne(g.standard_normal((G_v, case["d_c"], 12)) / math.sqrt(case["d_c"])).astype(np.float64)
+    exp_seqs, _ = _build(case)
+    o, _ = O.decode_explicit(case["q"], case["qr"], case["gq"], case["gk"], case["grq"], case["wk"],
+                             exp_seqs, 2, case["scale"], case["eps"])
+    out = O.up_project(o, wv)
+    H, G = case["H"], case["G"]
+    for b in range(2):
+        c_raw, r_raw = case["seqs_raw"][b]
+        ch = _torch_cache(torch.from_numpy(c_raw), "bf16")
+        rh = _torch_rope_key(r_raw, case["grk"], case["eps"], "bf16")
+        T = ch.shape[0]
+        for h in range(H):
+            k = F.rms_norm(ch @ torch.from_numpy(case["wk"][h // (H // G)].astype(np.float64)), (case["d_h"],),
+                           torch.from_numpy(case["gk"].astype(np.float64)), eps=case["eps"])
+            qh = F.rms_norm(torch.from_numpy(case["q"][b, :, h].astype(np.float64)), (case["d_h"],),
+                            torch.from_numpy(case["gq"].astype(np.float64)), eps=case["eps"])
+            qrh = F.rms_norm(torch.from_numpy(case["qr"][b, :, h].astype(np.float64)), (case["d_r"],),
+                             torch.from_numpy(case["grq"].astype(np.float64)), eps=case["eps"])
+            V = ch @ torch.from_numpy(wv[h // (H // G_v)])                      # materialised values [T, d_v]
+            mask = torch.ones(2, T, dtype=torch.bool)
+            for i in range(2):
+                mask[i, O.valid_length(T, 2, i):] = False
+            ref = F.scaled_dot_product_attention(torch.cat([qh, qrh], -1)[None, None],
+                                                 torch.cat([k, rh], -1)[None, None], V[None, None],
+                                                 attn_mask=mask, scale=case["scale"])[0, 0].numpy()
+            np.testing.assert_allclose(out[b, :, h], ref, rtol=1e-11, atol=1e-12)
+
+
+def test_mutation_up_projection_wrong_group_is_caught():
+    o = np.random.default_rng(82).standard_normal((3, 8, 16))
+    wv = np.random.default_rng(83).standard_normal((4, 16, 5))
+    ref = np.stack([o[:, h] @ wv[h // 2] for h in range(8)], axis=1)         # g(h) = h // (H / G_v)
+    np.testing.assert_allclose(O.up_project(o, wv), ref, rtol=1e-14)
+    bad = np.stack([o[:, h] @ wv[h % 4] for h in range(8)], axis=1)          # interleaved groups
+    assert np.max(np.abs(O.up_project(o, wv) - bad)) > 1e-3

@@ -118,6 +118,14 @@ def weights(w: Workload):
     return wk, gq, gk, grq, grk
 
 
+def value_weights(w: Workload, d_v: Optional[int] = None, G_v: Optional[int] = None) -> np.ndarray:
+    """W^V [G_v, d_c, d_v] ~ N(0, 1/d_c), fp32 (d_v defaults to d_h, G_v to G)."""
+    d_v = w.d_h if d_v is None else d_v
+    G_v = w.G if G_v is None else G_v
+    g = _rng(w.seed, 6)
+    return (g.standard_normal((G_v, w.d_c, d_v), dtype=np.float32) / np.float32(math.sqrt(w.d_c))).astype(np.float32)
+
+
 def sequence(w: Workload, b: int, length: Optional[int] = None):
     """Latents c [L, d_c] and raw post-RoPE keys r [L, d_r] of sequence b (fp32),
     with the outlier tokens already scaled."""
