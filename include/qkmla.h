@@ -138,6 +138,49 @@ int qkmla_append(const float* c_new, const float* k_rope_new, const float* w_k,
                  int d_c, int d_h, int d_r, float eps, unsigned flags, void* kv_cache,
                  int cache_dtype, void* ak_cache, int64_t num_slots, void* stream);
 
+/*
+ * qkmla_append_rope -- qkmla_append for RoPE keys that are not yet rotated:
+ * each new token's RoPE key is first rotated by its position, then normalised
+ * and stored exactly as qkmla_append stores a post-RoPE key.
+ * Source: as qkmla_append, and Technical Summary, Methodology, "Blockwise
+ * Normalization" (the RoPE part is a materialised vector normalised on its
+ * own; the normalised vector is the rotated one).
+ *
+ * Rotation (the original rotary formulation; the pages name none): interleaved
+ * pairs (x_2i, x_2i+1) of the d_r-vector turn by positions[n] * rope_theta^(-2i/d_r).
+ * Angles are reduced exactly enough for positions up to 2^24 (fp64 frequency,
+ * error-free fp32 product, two-part 2*pi reduction).
+ * k_rope_raw [N][d_r] fp32 (before rotation); positions [N] int32 device.
+ * Errors: as qkmla_append, and INVALID for a missing positions array, d_r odd
+ * or rope_theta <= 1; UNSUPPORTED for d_r > 64.
+ */
+int qkmla_append_rope(const float* c_new, const float* k_rope_raw, const int32_t* positions, float rope_theta,
+                      const float* w_k, const float* gamma_rope_k, const int64_t* slot_mapping, int N, int G,
+                      int d_c, int d_h, int d_r, float eps, unsigned flags, void* kv_cache, int cache_dtype,
+                      void* ak_cache, int64_t num_slots, void* stream);
+
+/*
+ * qkmla_project_query -- the query projection ahead of qkmla_absorb_query,
+ * with the RoPE rotation of the RoPE block fused in.
+ * Source: thelatestinai.com abstract (the static key weight is absorbed into
+ * the MLA query-side projection: the query comes from the layer input through
+ * W^Q, then qkmla_absorb_query folds gamma_q * gamma_k and W^K_g into it);
+ * Technical Summary, Methodology, "Blockwise Normalization".
+ *
+ *   [q_h | r_h] = x W^Q_h^T,  q[r][h] = q_h,  q_rope[r][h] = RoPE(r_h, positions[r])
+ *
+ * x [rows][d_x] bf16; w_q [H][d_h + d_r][d_x] bf16 (row j of W^Q_h holds output
+ * j's weights: the d_h content outputs, then the d_r RoPE outputs);
+ * positions [rows] int32 device (RoPE position of each query row);
+ * q [rows][H][d_h] fp32 (qkmla_absorb_query's input); q_rope [rows][H][d_r]
+ * fp32, rotated as in qkmla_append_rope, not normalised (qkmla_decode's input).
+ * Tensor cores, fp32 accumulation.  Errors: INVALID for null pointers, bad
+ * sizes or alignment, rope_theta <= 1 with d_r > 0; UNSUPPORTED for d_x % 64,
+ * odd d_h or d_r, d_r > 64, or d_h + d_r not in {96, 128, 160, 192, 256}.
+ */
+int qkmla_project_query(const void* x, const void* w_q, const int32_t* positions, float rope_theta, int rows,
+                        int d_x, int H, int d_h, int d_r, float* q, float* q_rope, void* stream);
+
 /* Arguments of qkmla_decode (plain pointers and sizes). */
 typedef struct qkmla_decode_args {
     const void* q_tilde;        /* [B][s_q][H][d_c] in cache_dtype (from absorb) */

@@ -29,6 +29,9 @@ full key caching", arXiv 2606.16310):
          MLA's latent decode path.
   [UP]   Technical Summary, "Problem Statement": MLA keeps the latent and
          recovers per-head quantities through up-projections (W^K_g for keys).
+  [QPROJ] thelatestinai.com abstract: the static key weight is absorbed into
+         the MLA query-side projection -- the query comes from the layer input
+         x through W^Q before the absorption.
 
 Readings where the pages are silent:
   * g(h) = h // (H/G) (contiguous head groups).
@@ -45,6 +48,10 @@ Readings where the pages are silent:
   * s_q > 1: query i of the step sees tokens t < seq_len - s_q + i + 1.
   * lse is the natural log of sum_t exp(l_t) with the logit scale included.
   * Plain-MLA mode (comparator): no norms, l = scale (q W^K_g^T . c^ + q_r . r^).
+  * RoPE (the pages name none): the original rotary formulation on interleaved
+    pairs, (x_2i, x_2i+1) rotated by pos * theta^(-2i/d_r); rotation comes
+    before the RMS normalisation of the RoPE block (the normalised vectors are
+    the rotated ones, as the post-RoPE inputs of the decode path).
   * Reduced-precision scalar cache (the scalar cache is the method's whole
     storage overhead: Technical Summary, Key Contributions and Results): alpha^k
     stored in IEEE half precision is the round-to-nearest-even fp16 of the fp32
@@ -59,6 +66,7 @@ __all__ = [
     "absorb_query", "append_tokens", "rope_key", "full_keys",
     "decode_explicit", "decode_absorbed", "combine_partials",
     "valid_length", "cache_write", "cache_gather", "up_project",
+    "rope_rotate", "project_query",
 ]
 
 
@@ -320,6 +328,33 @@ def up_project(o, w_v):
     for h in range(H):
         out[..., h, :] = o[..., h, :] @ w[g_of[h]]
     return out
+
+
+def rope_rotate(x, pos, theta: float):
+    """Rotary position embedding on interleaved pairs: (x_2i, x_2i+1) rotated by
+    the angle pos * theta^(-2i/d), d = x.shape[-1].  x [..., d]; pos broadcasts
+    against x[..., 0] (one position per vector).  fp64."""
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    inv_freq = np.power(float(theta), -np.arange(0, d, 2, dtype=np.float64) / d)      # [d/2]
+    ang = np.asarray(pos, np.float64)[..., None] * inv_freq                          # [..., d/2]
+    c, s = np.cos(ang), np.sin(ang)
+    out = np.empty_like(x)
+    out[..., 0::2] = x[..., 0::2] * c - x[..., 1::2] * s
+    out[..., 1::2] = x[..., 0::2] * s + x[..., 1::2] * c
+    return out
+
+
+def project_query(x, w_q, d_h: int, pos, theta: float):
+    """The query side before the absorption ([QPROJ]): q_h = x W^Q_h for every head.
+    x [R, d_x], w_q [H, d_h + d_r, d_x] (row j of W^Q_h holds output j's weights),
+    pos [R].  Returns q [R, H, d_h] (the content part) and q_rope [R, H, d_r]
+    (the RoPE part, rotated by each row's position; not normalised)."""
+    x = np.asarray(x, np.float64)
+    w = np.asarray(w_q, np.float64)
+    full = np.einsum("rk,hjk->rhj", x, w)
+    pos = np.asarray(pos)
+    return full[..., :d_h], rope_rotate(full[..., d_h:], pos[:, None], theta)
 
 
 # ----------------------------------------------------------------------------

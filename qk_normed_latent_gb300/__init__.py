@@ -28,7 +28,7 @@ FLAG_ALPHA_F16 = 8
 SYMBOLS = [
     "qkmla_absorb_query", "qkmla_append", "qkmla_decode_workspace_size", "qkmla_decode",
     "qkmla_get_device_status", "qkmla_status_string", "qkmla_version", "qkmla_decode_kernel_name",
-    "qkmla_decode_launch_count", "qkmla_up_project",
+    "qkmla_decode_launch_count", "qkmla_up_project", "qkmla_append_rope", "qkmla_project_query",
 ]
 
 
@@ -102,6 +102,10 @@ def lib() -> ctypes.CDLL:
         L.qkmla_decode_launch_count.restype = i
         L.qkmla_up_project.argtypes = [vp, i, vp, i, i, i, i, i, vp, i, vp]
         L.qkmla_up_project.restype = i
+        L.qkmla_append_rope.argtypes = [vp, vp, vp, f, vp, vp, vp, i, i, i, i, i, f, u, vp, i, vp, i64, vp]
+        L.qkmla_append_rope.restype = i
+        L.qkmla_project_query.argtypes = [vp, vp, vp, f, i, i, i, i, i, vp, vp, vp]
+        L.qkmla_project_query.restype = i
         if hasattr(L, "qkmla_decode_noalloc"):
             L.qkmla_decode_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), vp]
             L.qkmla_decode_noalloc.restype = i
@@ -211,6 +215,42 @@ def append(c_new, k_rope_new, w_k, gamma_rope_k, slot_mapping, kv_cache, ak_cach
     [num_slots, d_c+d_r] and ak_cache [num_slots, G] (fp32, or float16 for the
     reduced-precision scalar cache) at slot_mapping [N] (int64)."""
     prepare_append(c_new, k_rope_new, w_k, gamma_rope_k, slot_mapping, kv_cache, ak_cache, eps, plain)(stream)
+
+
+def prepare_append_rope(c_new, k_rope_raw, positions, rope_theta: float, w_k, gamma_rope_k, slot_mapping, kv_cache,
+                        ak_cache, eps: float, plain: bool = False) -> Prepared:
+    """qkmla_append_rope for fixed tensors: like prepare_append with unrotated RoPE
+    keys and their positions [N] (int32)."""
+    N, d_c = c_new.shape
+    d_r = k_rope_raw.shape[1]
+    G, _, d_h = w_k.shape
+    flags = (FLAG_PLAIN_MLA if plain else 0) | _alpha_flag(ak_cache)
+    return Prepared("qkmla_append_rope",
+                    (_ptr(c_new), _ptr(k_rope_raw), _ptr(positions), float(rope_theta), _ptr(w_k), _ptr(gamma_rope_k),
+                     _ptr(slot_mapping), N, G, d_c, d_h, d_r, float(eps), flags, _ptr(kv_cache),
+                     _dtype_code(kv_cache.dtype), _ptr(ak_cache), kv_cache.shape[0]))
+
+
+def append_rope(c_new, k_rope_raw, positions, rope_theta: float, w_k, gamma_rope_k, slot_mapping, kv_cache,
+                ak_cache, eps: float, plain: bool = False, stream=None):
+    """append() for RoPE keys before rotation: rotated by positions [N], then normalised and stored."""
+    prepare_append_rope(c_new, k_rope_raw, positions, rope_theta, w_k, gamma_rope_k, slot_mapping, kv_cache,
+                        ak_cache, eps, plain)(stream)
+
+
+def prepare_project_query(x, w_q, positions, rope_theta: float, q, q_rope) -> Prepared:
+    """qkmla_project_query for fixed tensors: x [rows, d_x] bf16, w_q [H, d_h + d_r, d_x] bf16,
+    positions [rows] int32 -> q [rows, H, d_h] fp32, q_rope [rows, H, d_r] fp32 (rotated)."""
+    rows, d_x = x.shape
+    H, d_h = q.shape[-2], q.shape[-1]
+    d_r = q_rope.shape[-1] if q_rope is not None else 0
+    return Prepared("qkmla_project_query", (_ptr(x), _ptr(w_q), _ptr(positions), float(rope_theta), rows, d_x, H,
+                                            d_h, d_r, _ptr(q), _ptr(q_rope)))
+
+
+def project_query(x, w_q, positions, rope_theta: float, q, q_rope, stream=None):
+    prepare_project_query(x, w_q, positions, rope_theta, q, q_rope)(stream)
+    return q, q_rope
 
 
 def make_decode_args(q_tilde, alpha_q, q_rope, gamma_rope_q, kv_cache, ak_cache, seq_lens, page_table,

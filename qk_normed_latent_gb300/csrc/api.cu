@@ -148,7 +148,27 @@ int qkmla_append(const float* c_new, const float* k_rope_new, const float* w_k, 
     if (!(eps >= 0.f)) return QKMLA_ERR_INVALID;
     const bool ak_f16 = !plain && (flags & QKMLA_FLAG_ALPHA_F16) != 0;
     return launch_append(c_new, k_rope_new, w_k, gamma_rope_k, slot_mapping, N, G, d_c, d_h, d_r, eps, plain,
-                         kv_cache, cache_dtype, ak_cache, ak_f16, num_slots, (cudaStream_t)stream);
+                         kv_cache, cache_dtype, ak_cache, ak_f16, num_slots, nullptr, 0.f, (cudaStream_t)stream);
+}
+
+int qkmla_append_rope(const float* c_new, const float* k_rope_raw, const int32_t* positions, float rope_theta,
+                      const float* w_k, const float* gamma_rope_k, const int64_t* slot_mapping, int N, int G, int d_c,
+                      int d_h, int d_r, float eps, unsigned flags, void* kv_cache, int cache_dtype, void* ak_cache,
+                      int64_t num_slots, void* stream) {
+    if (N > 0 && d_r > 0 && (!positions || !(rope_theta > 1.f) || d_r % 2)) return QKMLA_ERR_INVALID;
+    if (d_r > 64) return QKMLA_ERR_UNSUPPORTED;
+    const bool plain = (flags & QKMLA_FLAG_PLAIN_MLA) != 0;
+    if (N < 0 || G < 1 || d_c < 1 || d_h < 1 || d_r < 0 || num_slots < 1) return QKMLA_ERR_INVALID;
+    if (d_h > 256) return QKMLA_ERR_INVALID;
+    if (cache_dtype != QKMLA_F32 && cache_dtype != QKMLA_BF16) return QKMLA_ERR_UNSUPPORTED;
+    if (N == 0) return QKMLA_OK;
+    if (!c_new || !w_k || !slot_mapping || !kv_cache || !ak_cache) return QKMLA_ERR_INVALID;
+    if (d_r > 0 && !k_rope_raw) return QKMLA_ERR_INVALID;
+    if (!(eps >= 0.f)) return QKMLA_ERR_INVALID;
+    const bool ak_f16 = !plain && (flags & QKMLA_FLAG_ALPHA_F16) != 0;
+    return launch_append(c_new, k_rope_raw, w_k, gamma_rope_k, slot_mapping, N, G, d_c, d_h, d_r, eps, plain,
+                         kv_cache, cache_dtype, ak_cache, ak_f16, num_slots, d_r > 0 ? positions : nullptr,
+                         rope_theta, (cudaStream_t)stream);
 }
 
 size_t qkmla_decode_workspace_size(const qkmla_decode_args* a) {

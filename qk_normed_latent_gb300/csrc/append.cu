@@ -20,7 +20,11 @@
 // slice) and the normalised RoPE key.  Shapes or pointers the bulk copies cannot
 // take (d_c not a multiple of 64, misaligned bases) go to a plain-load kernel that
 // forms every key element with one fmaf chain over ascending k.
+//
+// With token positions (qkmla_append_rope) the RoPE key arrives unrotated: it is
+// rotated first (interleaved pairs, rope.cuh) and then normalised.
 #include "common.cuh"
+#include "rope.cuh"
 #include "tc_ptx.cuh"
 
 namespace qkmla {
@@ -57,23 +61,40 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
 }
 
 // Latent (pure cast) and RoPE key (normalised on its own) of token n into slot s.
+// (The whole warp calls it: the rotation pairs lanes j and j ^ 1.)
 template <typename CT>
 __device__ __forceinline__ void store_token(const float* lat, const float* __restrict__ r_new,
                                             const float* __restrict__ grk, int64_t n, int64_t s, int d_c, int d_r,
-                                            float eps, int plain, CT* __restrict__ kv, int lane) {
+                                            float eps, int plain, CT* __restrict__ kv, int lane, int pos,
+                                            const RopeFreq* freq) {
     CT* dst = kv + s * (int64_t)(d_c + d_r);
     for (int k = lane; k < d_c; k += 32) Elem<CT>::store(dst + k, lat[k]);
     const float* rs = r_new + n * d_r;
+    float rv[2];                                  // d_r <= 64: elements lane and lane + 32
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int j = lane + 32 * u;
+        rv[u] = j < d_r ? rs[j] : 0.f;
+        if (freq) {                               // rotate first, then normalise
+            const float w = __shfl_xor_sync(0xffffffffu, rv[u], 1);
+            if (j < d_r) {
+                float c, sn;
+                rope_cos_sin(pos, freq[j >> 1], &c, &sn);
+                rv[u] = rope_apply(j, rv[u], w, c, sn);
+            }
+        }
+    }
     float beta = 1.f;
     if (!plain) {
-        float ss = 0.f;
-        for (int j = lane; j < d_r; j += 32) ss = fmaf(rs[j], rs[j], ss);
-        ss = warp_sum(ss);
+        const float ss = warp_sum(fmaf(rv[0], rv[0], rv[1] * rv[1]));
         beta = 1.f / sqrtf(ss / (float)d_r + eps);
     }
-    for (int j = lane; j < d_r; j += 32) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int j = lane + 32 * u;
+        if (j >= d_r) continue;
         const float gmul = (plain || grk == nullptr) ? 1.f : grk[j];
-        Elem<CT>::store(dst + d_c + j, plain ? rs[j] : rs[j] * gmul * beta);
+        Elem<CT>::store(dst + d_c + j, plain ? rv[u] : rv[u] * gmul * beta);
     }
 }
 
@@ -84,8 +105,9 @@ __global__ void __cluster_dims__(S, 1, 1) __launch_bounds__(kThreads)
 append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r_new, const float* __restrict__ wk,
                     const float* __restrict__ grk, const int64_t* __restrict__ slots, int N, int G, int d_r,
                     float eps, int plain, CT* __restrict__ kv, void* __restrict__ ak, int ak_f16, int64_t num_slots,
-                    int* status) {
+                    const int32_t* __restrict__ positions, float theta, int* status) {
     using namespace tc;
+    __shared__ RopeFreq freq[32];
     constexpr int kDc = S * kKS, kDh = 16 * U;
     extern __shared__ __align__(128) uint8_t sm[];
     float* Cs = reinterpret_cast<float*>(sm);                              // [kFT][kKS]
@@ -103,6 +125,7 @@ append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r
         mbar_init(bar, 1);
         fence_barrier_init();
     }
+    if (positions && tid < d_r / 2) freq[tid] = rope_freq(theta, tid, d_r);
     __syncthreads();
     pdl_wait();
     pdl_trigger();
@@ -180,6 +203,19 @@ append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r
         }
         // the RoPE key, normalised on its own: the token's 16 threads hold its d_r values
         if (g == 0) {
+            if (positions) {                   // rotate first (pairs j, j ^ 1 in lanes q, q ^ 1)
+                const int pos = tok ? positions[n0 + t] : 0;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int j = q + 16 * v;
+                    const float w = __shfl_xor_sync(0xffffffffu, rv[v], 1);
+                    if (j < d_r) {
+                        float c, sn;
+                        rope_cos_sin(pos, freq[j >> 1], &c, &sn);
+                        rv[v] = rope_apply(j, rv[v], w, c, sn);
+                    }
+                }
+            }
             float sr = 0.f;
 #pragma unroll
             for (int v = 0; v < 4; ++v) sr = fmaf(rv[v], rv[v], sr);
@@ -204,13 +240,15 @@ __global__ void __launch_bounds__(kThreads)
 append_plain_kernel(const float* __restrict__ c_new, const float* __restrict__ r_new, const float* __restrict__ wk,
               const float* __restrict__ grk, const int64_t* __restrict__ slots, int N, int G, int d_c,
               int d_h, int d_r, float eps, int plain, CT* __restrict__ kv, void* __restrict__ ak, int ak_f16,
-              int64_t num_slots, int* status) {
+              int64_t num_slots, const int32_t* __restrict__ positions, float theta, int* status) {
     __shared__ float Cs[kTT][kKC + 1];
+    __shared__ RopeFreq freq[32];
     extern __shared__ float Ws[];              // [kKC][d_h]
     const int g = blockIdx.y;
     const int n0 = blockIdx.x * kTT;
     const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;   // ty: 0..7
     const int nj = (d_h + 31) / 32;
+    if (positions && tid < d_r / 2) freq[tid] = rope_freq(theta, tid, d_r);
     pdl_wait();
     pdl_trigger();
 
@@ -269,42 +307,44 @@ append_plain_kernel(const float* __restrict__ c_new, const float* __restrict__ r
     }
 
     if (g != 0) return;
+    __syncthreads();                              // freq (rotation) is written
     // latent (pure cast) and RoPE key (normalised separately), one warp per token
     for (int tl = ty; tl < kTT; tl += kThreads / 32) {
         const int n = n0 + tl;
         if (n >= N) break;
         const int64_t s = slots[n];
         if (s < 0 || s >= num_slots) continue;
-        store_token<CT>(c_new + (int64_t)n * d_c, r_new, grk, n, s, d_c, d_r, eps, plain, kv, tx);
+        store_token<CT>(c_new + (int64_t)n * d_c, r_new, grk, n, s, d_c, d_r, eps, plain, kv, tx,
+                        positions ? positions[n] : 0, positions ? freq : nullptr);
     }
 }
 
 template <typename CT, int S>
 cudaError_t launch_split(int U, const float* c_new, const float* r_new, const float* wk, const float* grk,
                          const int64_t* slots, int N, int G, int d_r, float eps, bool plain, CT* kv, void* ak,
-                         bool ak_f16, int64_t num_slots, cudaStream_t s) {
+                         bool ak_f16, int64_t num_slots, const int32_t* pos, float theta, cudaStream_t s) {
     auto k = U == 4 ? append_split_kernel<CT, S, 4> : append_split_kernel<CT, S, 8>;
     const int smem = split_smem_bytes(16 * U);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(((N + kFT - 1) / kFT) * S, G);
     return launch_pdl(k, grid, dim3(kThreads), smem, s, c_new, r_new, wk, grk, slots, N, G, d_r, eps, (int)plain, kv,
-                      ak, (int)ak_f16, num_slots, device_status_ptr());
+                      ak, (int)ak_f16, num_slots, pos, theta, device_status_ptr());
 }
 
 template <typename CT>
 int launch_t(const float* c_new, const float* r_new, const float* wk, const float* grk, const int64_t* slots, int N,
              int G, int d_c, int d_h, int d_r, float eps, bool plain, CT* kv, void* ak, bool ak_f16,
-             int64_t num_slots, cudaStream_t s) {
+             int64_t num_slots, const int32_t* pos, float theta, cudaStream_t s) {
     const int S = d_c / kKS;
     const bool split = d_c % kKS == 0 && (S == 2 || S == 4 || S == 8) && (d_h == 64 || d_h == 128) && d_r <= 64 &&
                        ((uintptr_t)c_new % 16) == 0 && ((uintptr_t)wk % 16) == 0;
     if (split) {
         const int U = d_h / 16;
         const cudaError_t e =
-            S == 2   ? launch_split<CT, 2>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, ak_f16, num_slots, s)
-            : S == 4 ? launch_split<CT, 4>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, ak_f16, num_slots, s)
-                     : launch_split<CT, 8>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, ak_f16, num_slots, s);
+            S == 2   ? launch_split<CT, 2>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, ak_f16, num_slots, pos, theta, s)
+            : S == 4 ? launch_split<CT, 4>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, ak_f16, num_slots, pos, theta, s)
+                     : launch_split<CT, 8>(U, c_new, r_new, wk, grk, slots, N, G, d_r, eps, plain, kv, ak, ak_f16, num_slots, pos, theta, s);
         if (e != cudaSuccess) return QKMLA_ERR_CUDA;
     } else {
         auto k = append_plain_kernel<CT>;
@@ -313,7 +353,7 @@ int launch_t(const float* c_new, const float* r_new, const float* wk, const floa
             return QKMLA_ERR_CUDA;
         dim3 grid((N + kTT - 1) / kTT, G);
         if (launch_pdl(k, grid, dim3(kThreads), smem, s, c_new, r_new, wk, grk, slots, N, G, d_c, d_h, d_r, eps,
-                       (int)plain, kv, ak, (int)ak_f16, num_slots, device_status_ptr()) != cudaSuccess)
+                       (int)plain, kv, ak, (int)ak_f16, num_slots, pos, theta, device_status_ptr()) != cudaSuccess)
             return QKMLA_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? QKMLA_OK : QKMLA_ERR_CUDA;
@@ -323,13 +363,14 @@ int launch_t(const float* c_new, const float* r_new, const float* wk, const floa
 
 int launch_append(const float* c_new, const float* r_new, const float* wk, const float* grk,
                   const int64_t* slots, int N, int G, int d_c, int d_h, int d_r, float eps, bool plain,
-                  void* kv, int cache_dtype, void* ak, bool ak_f16, int64_t num_slots, cudaStream_t s) {
+                  void* kv, int cache_dtype, void* ak, bool ak_f16, int64_t num_slots, const int32_t* positions,
+                  float rope_theta, cudaStream_t s) {
     if (N == 0) return QKMLA_OK;
     if (cache_dtype == QKMLA_F32)
         return launch_t<float>(c_new, r_new, wk, grk, slots, N, G, d_c, d_h, d_r, eps, plain, (float*)kv, ak,
-                               ak_f16, num_slots, s);
+                               ak_f16, num_slots, positions, rope_theta, s);
     return launch_t<__nv_bfloat16>(c_new, r_new, wk, grk, slots, N, G, d_c, d_h, d_r, eps, plain,
-                                   (__nv_bfloat16*)kv, ak, ak_f16, num_slots, s);
+                                   (__nv_bfloat16*)kv, ak, ak_f16, num_slots, positions, rope_theta, s);
 }
 
 }  // namespace qkmla

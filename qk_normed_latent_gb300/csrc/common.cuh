@@ -105,7 +105,8 @@ int launch_absorb_tc(const float* q, const float* gq, const float* gk, const flo
                      int d_h, int d_c, float eps, bool plain, void* qt, int qt_dtype, float* aq, cudaStream_t s);
 int launch_append(const float* c_new, const float* r_new, const float* wk, const float* grk,
                   const int64_t* slots, int N, int G, int d_c, int d_h, int d_r, float eps, bool plain,
-                  void* kv, int cache_dtype, void* ak, bool ak_f16, int64_t num_slots, cudaStream_t s);
+                  void* kv, int cache_dtype, void* ak, bool ak_f16, int64_t num_slots, const int32_t* positions,
+                  float rope_theta, cudaStream_t s);
 
 struct DecodePlan {
     int kernel;            // 0 = simt, 1 = tcgen05

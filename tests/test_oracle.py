@@ -563,3 +563,58 @@ def test_mutation_up_projection_wrong_group_is_caught():
     np.testing.assert_allclose(O.up_project(o, wv), ref, rtol=1e-14)
     bad = np.stack([o[:, h] @ wv[h % 4] for h in range(8)], axis=1)          # interleaved groups
     assert np.max(np.abs(O.up_project(o, wv) - bad)) > 1e-3
+
+
+# --------------------------------------------------------------------------
+# rotary position embedding and the query projection
+# --------------------------------------------------------------------------
+def test_rope_rotation_matches_complex_multiplication():
+    """Interleaved pairs as complex numbers times e^{i pos theta^(-2k/d)} (torch polar)."""
+    g = np.random.default_rng(90)
+    x = g.standard_normal((7, 3, 16))
+    pos = g.integers(0, 200000, size=(7, 3))
+    got = O.rope_rotate(x, pos, 10000.0)
+    xc = torch.view_as_complex(torch.from_numpy(x.reshape(7, 3, 8, 2).copy()))
+    freq = torch.tensor(10000.0, dtype=torch.float64) ** (-torch.arange(0, 16, 2, dtype=torch.float64) / 16)
+    rot = torch.polar(torch.ones(7, 3, 8, dtype=torch.float64), torch.from_numpy(pos).double()[..., None] * freq)
+    ref = torch.view_as_real(xc * rot).reshape(7, 3, 16).numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_rope_rotation_invariants():
+    g = np.random.default_rng(91)
+    q, k = g.standard_normal((2, 32))
+    # a rotation: norms (hence the RMS statistic) are preserved
+    np.testing.assert_allclose(np.linalg.norm(O.rope_rotate(q, 1234, 500.0)), np.linalg.norm(q), rtol=1e-13)
+    # position 0 is the identity
+    np.testing.assert_allclose(O.rope_rotate(q, 0, 500.0), q, rtol=0, atol=0)
+    # relative position: <R(m) q, R(n) k> depends on m - n only
+    a = O.rope_rotate(q, 700, 500.0) @ O.rope_rotate(k, 300, 500.0)
+    b = O.rope_rotate(q, 1400, 500.0) @ O.rope_rotate(k, 1000, 500.0)
+    np.testing.assert_allclose(a, b, rtol=1e-10)
+    # d = 2: one rotation by pos (theta^0 = 1)
+    v = O.rope_rotate(np.array([1.0, 0.0]), 0.5, 10000.0)
+    np.testing.assert_allclose(v, [math.cos(0.5), math.sin(0.5)], rtol=1e-15)
+
+
+def test_mutation_rope_half_split_pairs_are_caught():
+    """The other common convention pairs x_i with x_{i+d/2}; it is a different map."""
+    g = np.random.default_rng(92)
+    x = g.standard_normal(16)
+    d = 16
+    inv = 10000.0 ** (-np.arange(0, d, 2) / d)
+    ang = 77 * inv
+    half = np.concatenate([x[:8] * np.cos(ang) - x[8:] * np.sin(ang), x[:8] * np.sin(ang) + x[8:] * np.cos(ang)])
+    assert np.max(np.abs(O.rope_rotate(x, 77, 10000.0) - half)) > 1e-3
+
+
+def test_project_query_matches_torch_linear():
+    g = np.random.default_rng(93)
+    x = g.standard_normal((5, 48))
+    w = g.standard_normal((4, 24 + 8, 48))
+    pos = g.integers(0, 5000, size=5)
+    q, qr = O.project_query(x, w, 24, pos, 10000.0)
+    full = torch.nn.functional.linear(torch.from_numpy(x), torch.from_numpy(w.reshape(-1, 48))).reshape(5, 4, 32).numpy()
+    np.testing.assert_allclose(q, full[..., :24], rtol=1e-13, atol=1e-13)
+    for r in range(5):
+        np.testing.assert_allclose(qr[r], O.rope_rotate(full[r, :, 24:], pos[r], 10000.0), rtol=1e-13, atol=1e-13)

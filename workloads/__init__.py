@@ -126,6 +126,15 @@ def value_weights(w: Workload, d_v: Optional[int] = None, G_v: Optional[int] = N
     return (g.standard_normal((G_v, w.d_c, d_v), dtype=np.float32) / np.float32(math.sqrt(w.d_c))).astype(np.float32)
 
 
+def query_inputs(w: Workload, d_x: int):
+    """The layer input of the step's query rows x [B, s_q, d_x] ~ N(0,1) and the query
+    projection W^Q [H, d_h + d_r, d_x] ~ N(0, 1/d_x) (content rows, then RoPE rows), fp32."""
+    g = _rng(w.seed, 7)
+    x = g.standard_normal((w.B, w.s_q, d_x), dtype=np.float32)
+    wq = (g.standard_normal((w.H, w.d_h + w.d_r, d_x), dtype=np.float32) / np.float32(math.sqrt(d_x))).astype(np.float32)
+    return x, wq
+
+
 def sequence(w: Workload, b: int, length: Optional[int] = None):
     """Latents c [L, d_c] and raw post-RoPE keys r [L, d_r] of sequence b (fp32),
     with the outlier tokens already scaled."""
