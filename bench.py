@@ -439,6 +439,31 @@ def main():
                   "algorithmic_bytes": up_bytes, "algorithmic_flops": up_flops}
     del up_g
 
+    # the query projection from the layer input with its RoPE rotation (its own call, timed
+    # alone): d_x = 1536 for the 128-head shape (the DeepSeek-V3 query down-projection
+    # width), 4 d_h otherwise
+    d_x = 1536 if w.H == 128 else 4 * w.d_h
+    xq, wq = W.query_inputs(w, d_x)
+    xq_d = torch.from_numpy(xq.reshape(w.rows, d_x)).to("cuda").to(torch.bfloat16)
+    wq_d = torch.from_numpy(wq).to("cuda").to(torch.bfloat16)
+    pos_d = torch.from_numpy(np.array([int(lens[b]) - w.s_q + i for b in range(w.B) for i in range(w.s_q)],
+                                      dtype=np.int32)).to("cuda")
+    pq_q = torch.empty((w.rows, w.H, w.d_h), dtype=torch.float32, device="cuda")
+    pq_r = torch.empty((w.rows, w.H, w.d_r), dtype=torch.float32, device="cuda")
+    pq_call = Q.prepare_project_query(xq_d, wq_d, pos_d, 10000.0, pq_q, pq_r)
+    pq_g = capture(lambda: pq_call())
+    pq_ms = statistics.median(timed(pq_g, min(args.steps, 100)))
+    if Q.get_device_status() != 0:
+        raise RuntimeError("device status error in the projection timing")
+    pq_flops = 2 * w.rows * d_x * w.H * (w.d_h + w.d_r)
+    pq_bytes = w.rows * d_x * 2 + wq.size * 2 + w.rows * w.H * (w.d_h + w.d_r) * 4
+    project_query = {"ms": pq_ms, "d_x": d_x, "tflops": pq_flops / (pq_ms * 1e-3) / 1e12,
+                     "gbs": pq_bytes / (pq_ms * 1e-3) / 1e9,
+                     "frac_of_bf16": pq_flops / (pq_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+                     "frac_of_hbm": pq_bytes / (pq_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                     "algorithmic_flops": pq_flops, "algorithmic_bytes": pq_bytes}
+    del pq_g
+
     # end to end through the public API with host buffers: H2D of the step's inputs,
     # the three calls, D2H of o and lse, all inside the timed region.  The inputs
     # (q, q_rope and the step's new tokens) live in one pinned host buffer and one
@@ -485,6 +510,7 @@ def main():
             "plain_mla": plain,
             "alpha_f16": alpha_f16,
             "up_project": up_project,
+            "project_query": project_query,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,

@@ -273,15 +273,21 @@ int qkmla_decode_launch_count(const qkmla_decode_args* a);
  * Same arguments and results as qkmla_decode, except that `workspace` and
  * `workspace_bytes` are ignored: the split-KV partials and scheduler data live
  * in a fixed array of qkmla_decode_noalloc_max_workspace() bytes (64 MiB)
- * inside the library, held on every GPU where it is used until the process
- * exits.  The call allocates nothing.  Arguments needing more scratch than
- * that return QKMLA_ERR_WORKSPACE before anything is launched.
+ * inside the library.  The array is part of the library's device code, so it
+ * is reserved on a GPU when that code is loaded there -- with CUDA's default
+ * lazy loading, at the first launch of any of the library's kernels on that
+ * device; with CUDA_MODULE_LOADING=EAGER, when a context is created -- and is
+ * held until the process exits.  The call allocates nothing.  Arguments
+ * needing more scratch than that return QKMLA_ERR_WORKSPACE before anything is
+ * launched.
  * The first call on a device resolves the array's address on that device (it
- * must be current); make that first call before any stream capture.  All
- * calls on a device share the array: calls whose kernels can overlap on the
- * GPU (different streams with no ordering between them) race on it.  The
- * array keeps the previous call's contents; decode writes every scratch entry
- * it reads, so nothing needs to start at zero.
+ * must be current) and keeps it for the process; make that first call before
+ * any stream capture, and do not use the library across a cudaDeviceReset
+ * (the kept address would be stale).  All calls on a device share the array:
+ * calls whose kernels can overlap on the GPU (different streams with no
+ * ordering between them) race on it.  The array keeps the previous call's
+ * contents; decode writes every scratch entry it reads, so nothing needs to
+ * start at zero.
  */
 int qkmla_decode_noalloc(const qkmla_decode_args* a, void* stream);
 

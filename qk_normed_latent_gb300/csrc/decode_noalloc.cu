@@ -7,12 +7,15 @@
 // would synchronise or fail under memory pressure).  This entry point takes
 // the same arguments as qkmla_decode but ignores `workspace` /
 // `workspace_bytes`: the split-KV partials and scheduler metadata live in a
-// fixed, file-scope device array that every GPU loading this library holds
-// until the process exits.
+// fixed, file-scope device array.  It belongs to the library's device code, so
+// a GPU reserves it when that code is loaded there (CUDA's default lazy
+// loading: at the first launch of any kernel of this library on the device;
+// eager loading: at context creation) and holds it until the process exits.
 //
 // The first call on a device resolves the array's device address with
-// cudaGetSymbolAddress (with that device current) and caches it; make that
-// first call before any stream capture.  All calls on a device share the one
+// cudaGetSymbolAddress (with that device current) and keeps it for the
+// process; make that first call before any stream capture, and do not use the
+// library across a cudaDeviceReset (the kept address would be stale).  All calls on a device share the one
 // array, so calls whose kernels overlap on the GPU (different streams without
 // ordering) race on it; calls serialised on one stream are fine.  The array
 // keeps the previous call's contents; the decode path writes every scheduler

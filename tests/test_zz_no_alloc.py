@@ -35,25 +35,44 @@ def _close(a, b):
     assert np.linalg.norm(a - b) <= 5e-3 * max(np.linalg.norm(b), 1e-30)
 
 
-@pytest.mark.parametrize("name,widx,lens", [
-    ("dsv3_B4", 2, (4096, 1000, 20000, 64)),
-    ("small_B3", 1, (1024, 5000, 8192)),
+def _dirty_scratch(Q):
+    """A no-alloc call of another shape first, so the shared array holds stale
+    scheduler entries and partials when the checked calls run."""
+    from qk_normed_latent_gb300.pipeline import DeviceState
+    w = W.small(W.WORKLOADS[1], 5, (700, 64, 9000, 3000, 131))
+    st = DeviceState(w)
+    st.absorb()
+    st.append_step()
+    a = st.decode_args(num_splits=7)
+    rc = Q.lib().qkmla_decode_noalloc(ctypes.byref(a), Q._stream(None))
+    assert rc == Q.OK, Q.status_string(rc)
+    assert Q.get_device_status() == 0
+
+
+@pytest.mark.parametrize("name,widx,lens,splits", [
+    ("dsv3_B4", 2, (4096, 1000, 20000, 64), 0),
+    ("small_B3", 1, (1024, 5000, 8192), 0),
+    # more than 128 sequences: the scheduler kernel's items and split lists live in the array too
+    ("small_B160_sched", 1, tuple(16 + (37 * i) % 600 for i in range(160)), 0),
+    # the CUDA-core kernel's split partials (fp32 latent cache)
+    ("tiny_fp32_split", 0, (256, 77), 4),
 ])
-def test_noalloc_matches_workspace_entry_point_twice(Q, name, widx, lens):
+def test_noalloc_matches_workspace_entry_point_twice(Q, name, widx, lens, splits):
     from qk_normed_latent_gb300.pipeline import DeviceState
     w = W.small(W.WORKLOADS[widx], len(lens), lens)
     st = DeviceState(w)
     st.absorb()
     st.append_step()
-    st.decode()                                   # existing entry point, torch workspace
+    st.decode(num_splits=splits)                  # existing entry point, torch workspace
     assert Q.get_device_status() == 0
     o_ref = st.o.float().cpu().numpy().copy()
     l_ref = st.lse.cpu().numpy().copy()
     assert Q.decode_workspace_size(st.args) > 0   # this case does use scratch
+    _dirty_scratch(Q)
     for _ in range(2):
         st.o.fill_(float("nan"))
         st.lse.fill_(float("nan"))
-        a = st.decode_args()
+        a = st.decode_args(num_splits=splits)
         a.workspace, a.workspace_bytes = None, 0  # ignored by the no-alloc entry point
         rc = Q.lib().qkmla_decode_noalloc(ctypes.byref(a), Q._stream(None))
         assert rc == Q.OK, Q.status_string(rc)
