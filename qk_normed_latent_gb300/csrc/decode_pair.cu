@@ -343,19 +343,21 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 const bool got_s = __all_sync(0xffffffffu, wait_bounded(sfull, j & 1, p.status));
                 tc_fence_after();
                 const void* ak_t = sm + kOffStage + s * kStageB + kSLat + kSRope;
+                {
+                    // every load first, one wait: a single TMEM round trip per tile
+                    uint32_t sc[kT], sr[PLAIN ? 1 : kT];
 #pragma unroll
-                for (int c = 0; c < kT / 16; ++c) {
-                    uint32_t sc[16], sr[16];
-                    tmem_ld16(tmem + kCSc + lane_base + 16 * c, sc);
-                    if (!PLAIN) tmem_ld16(tmem + kCSr + lane_base + 16 * c, sr);
+                    for (int c = 0; c < kT / 16; ++c) {
+                        tmem_ld16(tmem + kCSc + lane_base + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(sc + 16 * c));
+                        if (!PLAIN)
+                            tmem_ld16(tmem + kCSr + lane_base + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(sr + 16 * c));
+                    }
                     tmem_wait_ld();
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int t = 16 * c + jj;
-                        pv[t] = PLAIN ? rs * __uint_as_float(sc[jj])
-                                      : fmaf(coef * load_alpha<AKH>(ak_t, t * p.G + g), __uint_as_float(sc[jj]),
-                                             __uint_as_float(sr[jj]));
-                    }
+                    for (int t = 0; t < kT; ++t)
+                        pv[t] = PLAIN ? rs * __uint_as_float(sc[t])
+                                      : fmaf(coef * load_alpha<AKH>(ak_t, t * p.G + g), __uint_as_float(sc[t]),
+                                             __uint_as_float(sr[PLAIN ? 0 : t]));
                 }
                 tc_fence_before();
                 __syncwarp();
