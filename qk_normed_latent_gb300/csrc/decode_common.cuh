@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -156,6 +157,8 @@ __device__ __forceinline__ void bulk_copy_to_cta(uint32_t remote_dst, const void
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk copy has finished READING its source.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk copy has completed (its writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Relaxed remote arrive: only orders this thread's earlier READS of the rows the
 // other CTA will overwrite (their values are already consumed), no release fence.
 // `dep` is a value computed from every read that must complete first; taking it
@@ -172,6 +175,7 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 // Host side, shared by the launchers.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();   // the driver's tensor-map encoder (nullptr if absent)
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int row_elems, int box_cols, int box_rows,
               CUtensorMapSwizzle sw);
 int launch_pair(const qkmla_decode_args* a, const TcParams& tp, int max_items, cudaStream_t s);

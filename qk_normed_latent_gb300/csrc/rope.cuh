@@ -26,8 +26,10 @@ __device__ __forceinline__ RopeFreq rope_freq(float theta, int i, int d) {
     return r;
 }
 
-// cos and sin of pos * f.
-__device__ __forceinline__ void rope_cos_sin(int pos, RopeFreq f, float* c, float* s) {
+// cos and sin of pos * f.  Kept out of line: sincosf carries a large slow path
+// (for arguments far beyond this reduced range), and one copy per unrolled use
+// would overflow the instruction cache of the kernels that rotate many pairs.
+static __device__ __noinline__ void rope_cos_sin(int pos, RopeFreq f, float* c, float* s) {
     constexpr float kTwoPiHi = 6.2831854820251465f;      // 2 pi rounded to fp32
     constexpr float kTwoPiLo = -1.7484555314695172e-07f;  // 2 pi - kTwoPiHi
     constexpr float kInvTwoPi = 0.15915493667125702f;
@@ -39,6 +41,26 @@ __device__ __forceinline__ void rope_cos_sin(int pos, RopeFreq f, float* c, floa
     r = fmaf(-k, kTwoPiLo, r);
     r += ae;
     sincosf(r, s, c);
+}
+
+// cos and sin of pos * f for four frequencies at once: four independent chains,
+// so their latencies overlap (the kernels that rotate many pairs per thread call
+// this instead of four rope_cos_sin).
+static __device__ __noinline__ void rope_cos_sin4(int pos, const RopeFreq* f, float* c, float* s) {
+    constexpr float kTwoPiHi = 6.2831854820251465f;
+    constexpr float kTwoPiLo = -1.7484555314695172e-07f;
+    constexpr float kInvTwoPi = 0.15915493667125702f;
+    const float P = (float)pos;
+    float r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float a = P * f[i].hi;
+        const float ae = fmaf(P, f[i].hi, -a) + P * f[i].lo;
+        const float k = rintf(a * kInvTwoPi);
+        r[i] = fmaf(-k, kTwoPiLo, fmaf(-k, kTwoPiHi, a)) + ae;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sincosf(r[i], &s[i], &c[i]);
 }
 
 // One interleaved pair's rotation: element j (= 2i or 2i+1) of the rotated

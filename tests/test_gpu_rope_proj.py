@@ -29,6 +29,7 @@ def Q():
     (256, 1536, 128, 128, 64),    # two query tokens x 128 sequences, DeepSeek-V3 shape
     (5, 256, 16, 64, 32),         # the small model, a ragged row tile
     (130, 512, 8, 128, 0),        # no RoPE block
+    (7, 128, 4, 80, 16),          # d_h not a multiple of 32: the threads store their rows
 ])
 def test_project_query_matches_oracle(Q, rows, d_x, H, d_h, d_r):
     g = np.random.default_rng(rows + d_x)

@@ -28,6 +28,7 @@ def Q():
     (256, 128, 8, 512, 128),      # two query tokens x 128 sequences, DeepSeek-V3 shape
     (3, 8, 8, 128, 192),          # one matrix per head
     (70, 16, 2, 64, 256),
+    (3, 192, 1, 128, 64),         # 192 heads a group: two head blocks, the threads store their rows
 ])
 @pytest.mark.parametrize("o_dt", ["f32", "bf16"])
 @pytest.mark.parametrize("out_dt", ["f32", "bf16"])
