@@ -441,96 +441,125 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
 #pragma unroll
                     for (int t = 0; t < kT; ++t) lg[t] = __uint_as_float(v[t]);
                 }
+                const float m_own = y_off[lane];          // group A's row maximum of these partials
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ownfree);
-                // ---- + the other CTA's ----
-                const bool got_x =
-                    __all_sync(0xffffffffu, got_own && wait_bounded_cluster(&xfull[sub], j & 1, p.status));
-                if (got_x) {
-                    const float off = x_off[lane];
-#pragma unroll
-                    for (int c8 = 0; c8 < kT / 8; ++c8) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(sX + xrow + ((c8 ^ (lane & 7)) << 4));
-                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[u]));
-                            lg[8 * c8 + 2 * u] += off + f.x;
-                            lg[8 * c8 + 2 * u + 1] += off + f.y;
-                        }
-                    }
-                }
-                if (!got_x) { ok = false; *(volatile int*)abort_flag = 1; break; }
-                if (valid < kT) {
-#pragma unroll
-                    for (int t = 0; t < kT; ++t)
-                        if (t >= valid) lg[t] = -INFINITY;
-                }
-                float mx[8];                                   // tree max: short dependency chains
-#pragma unroll
-                for (int q = 0; q < 8; ++q) mx[q] = fmaxf(fmaxf(lg[q], lg[q + 8]), fmaxf(lg[q + 16], lg[q + 24]));
-#pragma unroll
-                for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], fmaxf(fmaxf(lg[q + 32], lg[q + 40]), fmaxf(lg[q + 48], lg[q + 56])));
-                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                // every X value has been read (mt depends on all of them): arm for the next
-                // tile and let the other CTA overwrite these rows
-                const float mt_w = warp_max(mt);
-                if (lane == 0 && j + 1 < n_t) {
-                    mbar_arrive_expect_tx(&xfull[sub], kXSlice);
-                    mbar_arrive_remote_relaxed(peer_xfree, mt_w);
-                }
-                // lazy running max: move it only when the tile max exceeds it by > 8 (log2)
-                float corr = 1.f;
-                const bool need = mt > m_run + 8.f;
-                if (need) {
-                    corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mt);
-                    m_run = mt;
-                }
-                // TMEM loads/stores are warp-collective: the whole warp rescales when any
-                // of its rows needs it, each lane by its own factor (1 for the others)
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
-                    // the previous tile's output MMA: its P buffer's barrier, whose earlier
-                    // phases this warp has consumed (so the parity names one phase)
-                    const bool got_o =
-                        __all_sync(0xffffffffu, wait_bounded(&pdone[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status));
-                    if (!got_o) { ok = false; *(volatile int*)abort_flag = 1; break; }
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int c16 = 0; c16 < kHalfLat; c16 += 16) {
-                        uint32_t v[16];
-                        tmem_ld16(tmem + kCO + c16 + lane_base, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) * corr);
-                        tmem_st16(tmem + kCO + c16 + lane_base, v);
-                    }
-                    tmem_wait_st();
-                }
-                l_run *= corr;
                 // P (bf16) into TMEM buffer pb once the output MMA two tiles back released it
                 if (j >= 2) {
                     const bool got_p = __all_sync(0xffffffffu, wait_bounded(&pdone[pb], ((j >> 1) - 1) & 1, p.status));
                     if (!got_p) { ok = false; *(volatile int*)abort_flag = 1; break; }
                     tc_fence_after();
                 }
-                float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+                // ---- + the other CTA's ----
+                const bool got_x =
+                    __all_sync(0xffffffffu, got_own && wait_bounded_cluster(&xfull[sub], j & 1, p.status));
+                if (!got_x) { ok = false; *(volatile int*)abort_flag = 1; break; }
+                const float off = x_off[lane];
+                uint32_t xw[kT / 2];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t w16[16];
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const float e0 = fast_exp2(lg[32 * h + 2 * q] - m_run);
-                        const float e1 = fast_exp2(lg[32 * h + 2 * q + 1] - m_run);
-                        ps4[q & 3] += e0 + e1;
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
-                        w16[q] = *reinterpret_cast<const uint32_t*>(&b2);
-                    }
-                    tmem_st16(tmem + kCP + pb * (kT / 2) + 16 * h + lane_base, w16);
+                for (int c8 = 0; c8 < kT / 8; ++c8) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(sX + xrow + ((c8 ^ (lane & 7)) << 4));
+                    xw[4 * c8] = v.x; xw[4 * c8 + 1] = v.y; xw[4 * c8 + 2] = v.z; xw[4 * c8 + 3] = v.w;
                 }
-                tmem_wait_st();
-                l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+                {
+                    // every X value has been read: arm for the next tile and let the other CTA
+                    // overwrite these rows
+                    uint32_t xdep = __float_as_uint(off);
+#pragma unroll
+                    for (int u = 0; u < kT / 2; ++u) xdep ^= xw[u];
+                    const uint32_t xdep_w = __reduce_xor_sync(0xffffffffu, xdep);
+                    if (lane == 0 && j + 1 < n_t) {
+                        mbar_arrive_expect_tx(&xfull[sub], kXSlice);
+                        mbar_arrive_remote_relaxed(peer_xfree, __uint_as_float(xdep_w));
+                    }
+                }
+                // own max + partner max bounds the tile max: when it cannot move the running
+                // max (by > 8, log2) for any row of the warp and the tile is full, the sums go
+                // straight into the exponentials
+                const bool fast = __all_sync(0xffffffffu, valid == kT && m_own + off <= m_run + 8.f);
+                float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+                if (fast) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t w16[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const int t = 32 * h + 2 * q;
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[t >> 1]));
+                            const float e0 = fast_exp2(lg[t] + (off + f.x) - m_run);
+                            const float e1 = fast_exp2(lg[t + 1] + (off + f.y) - m_run);
+                            ps4[q & 3] += e0 + e1;
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
+                            w16[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                        }
+                        tmem_st16(tmem + kCP + pb * (kT / 2) + 16 * h + lane_base, w16);
+                    }
+                    tmem_wait_st();
+                    l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < kT; t += 2) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[t >> 1]));
+                        lg[t] += off + f.x;
+                        lg[t + 1] += off + f.y;
+                    }
+                    if (valid < kT) {
+#pragma unroll
+                        for (int t = 0; t < kT; ++t)
+                            if (t >= valid) lg[t] = -INFINITY;
+                    }
+                    float corr = 1.f;
+                    bool need = false;
+                    if (m_own + off > m_run + 8.f) {
+                        float mx[8];                           // tree max: short dependency chains
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) mx[q] = fmaxf(fmaxf(lg[q], lg[q + 8]), fmaxf(lg[q + 16], lg[q + 24]));
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], fmaxf(fmaxf(lg[q + 32], lg[q + 40]), fmaxf(lg[q + 48], lg[q + 56])));
+                        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                        need = mt > m_run + 8.f;
+                        if (need) {
+                            corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mt);
+                            m_run = mt;
+                        }
+                    }
+                    // TMEM loads/stores are warp-collective: the whole warp rescales when any
+                    // of its rows needs it, each lane by its own factor (1 for the others)
+                    if (j > 0 && __any_sync(0xffffffffu, need)) {
+                        const bool got_o =
+                            __all_sync(0xffffffffu, wait_bounded(&pdone[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status));
+                        if (!got_o) { ok = false; *(volatile int*)abort_flag = 1; break; }
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c16 = 0; c16 < kHalfLat; c16 += 16) {
+                            uint32_t v[16];
+                            tmem_ld16(tmem + kCO + c16 + lane_base, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) * corr);
+                            tmem_st16(tmem + kCO + c16 + lane_base, v);
+                        }
+                        tmem_wait_st();
+                    }
+                    l_run *= corr;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t w16[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const float e0 = fast_exp2(lg[32 * h + 2 * q] - m_run);
+                            const float e1 = fast_exp2(lg[32 * h + 2 * q + 1] - m_run);
+                            ps4[q & 3] += e0 + e1;
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
+                            w16[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                        }
+                        tmem_st16(tmem + kCP + pb * (kT / 2) + 16 * h + lane_base, w16);
+                    }
+                    tmem_wait_st();
+                    l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+                }
                 if (valid < kT) {   // zero this CTA's latent rows past the sequence end (this warp's share)
                     uint8_t* stg = sm + kOffStage + s * kStageB;
                     const int nrow = kT - valid;
