@@ -111,10 +111,10 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
     float* coef_s = (float*)(sm + kOffMisc + kNumBars * 8 + 16);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    pdl_wait();
-    pdl_trigger();
     WorkItem it;
     int seq_len;
+    // the in-kernel plan reads only seq_lens, which no kernel of the call writes: it
+    // is made before the dependency wait, overlapping the previous kernel's tail
     if (p.sched_inline) {                                // both CTAs derive the same plan
         __shared__ SchedSmem S;
         compute_schedule(p.seq_lens, p.B, p.s_q, p.sa, S, p.status, blockIdx.x == 0 && blockIdx.y == 0);
@@ -122,6 +122,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
         it = schedule_item(S, p.B, (int)blockIdx.y);
         seq_len = S.len[it.b];                           // the plan's copy
     } else {
+        pdl_wait();                                      // the scheduler kernel's items
         if ((int)blockIdx.y >= *p.n_items) return;       // uniform over the cluster
         it = p.items[blockIdx.y];
         seq_len = p.seq_lens[it.b];
@@ -153,6 +154,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
+    pdl_wait();                // q~, alpha^q, the RoPE query and the cache are written by earlier kernels
+    pdl_trigger();
     // ---- prologue: this CTA's half of Q~ (TMA, four 64-column boxes) and of the
     //      normalised RoPE query ----
     const size_t qrow0 = ((size_t)b * p.s_q + qi) * p.H;

@@ -124,10 +124,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int item_idx = blockIdx.y;
-    pdl_wait();
-    pdl_trigger();
     WorkItem it;
     int seq_len;
+    // the in-kernel plan reads only seq_lens, which no kernel of the call writes: it
+    // is made before the dependency wait, overlapping the previous kernel's tail
     if (p.sched_inline) {
         __shared__ SchedSmem S;
         compute_schedule(p.seq_lens, p.B, p.s_q, p.sa, S, p.status, item_idx == 0 && blockIdx.x == 0);
@@ -135,6 +135,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
         it = schedule_item(S, p.B, item_idx);
         seq_len = S.len[it.b];                     // the plan's copy: no second trip to memory
     } else {
+        pdl_wait();                                // the scheduler kernel's items
         if (item_idx >= *p.n_items) return;
         it = p.items[item_idx];
         seq_len = p.seq_lens[it.b];
@@ -169,6 +170,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
         prefetch_tmap(&tm_q);
     }
     __syncthreads();
+    pdl_wait();                                    // q~, alpha^q and the cache are written by earlier kernels
+    pdl_trigger();
     const size_t qrow0 = ((size_t)b * p.s_q + qi) * p.H + h0;
 
     // ---- TMA producer state (warp 0): the slot of tile j + lane, 32 tiles at a time ----
