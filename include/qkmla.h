@@ -39,6 +39,16 @@
  *    sequence).
  *  - The library is stateless apart from the status word and a small per-
  *    device table of launch limits; it is thread-safe.
+ *  - Every kernel is launched with programmatic stream serialization and lets
+ *    the next kernel of the stream launch early.  Its writes, and its reads of
+ *    anything a kernel of this library produces (q~, alpha^q, the cache, q and
+ *    q_rope of qkmla_project_query, o), wait for the previous kernel of the
+ *    stream.  Reads of inputs no kernel of the library writes may start
+ *    earlier: seq_lens in qkmla_decode; W^K, the new tokens, their slots and
+ *    positions in qkmla_append / qkmla_append_rope.  A previous kernel that
+ *    itself signals early dependent launch must therefore not be writing
+ *    those inputs (kernels that do not signal it, and copies, are waited for
+ *    in full as usual).
  */
 #ifndef QKMLA_H
 #define QKMLA_H

@@ -127,8 +127,10 @@ append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r
     }
     if (positions && tid < d_r / 2) freq[tid] = rope_freq(theta, tid, d_r);
     __syncthreads();
-    pdl_wait();
     pdl_trigger();
+    // Every input (the weights, the new tokens, their slots and positions) is one no
+    // kernel of this library writes, so the loads and the partial keys run before the
+    // dependency wait, overlapping the previous kernel; only the cache writes wait.
     if (tid == 0) {
         mbar_arrive_expect_tx(bar, (uint32_t)((nvalid * kKS + kKS * kDh) * 4));
         bulk_load(Ws, wk + ((int64_t)g * kDc + k0) * kDh, (uint32_t)(kKS * kDh * 4), bar);
@@ -172,6 +174,7 @@ append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) red[t * kDh + q + 16 * u] = acc[u];
+    pdl_wait();                            // the cache writes follow the previous kernel
     const bool slot_ok = tok && slot >= 0 && slot < num_slots;
     // g = 0: this CTA's slice of the token's latent (a pure cast)
     if (g == 0 && all_ok && slot_ok) {
