@@ -142,10 +142,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
     }
     const int rows_o = p.rows_o;
     const int row0 = blockIdx.x * rows_o;          // row index within the sequence's s_q*H rows
-    const int qi = row0 / p.H, h0 = row0 % p.H;
+    const int qi = row0 / p.H, h0 = row0 % p.H;    // the first row's query token and head
     const int b = it.b;
     const bool bad = seq_len < p.s_q || seq_len > p.max_pages * p.page_size;
-    const int L = bad ? 0 : seq_len - p.s_q + qi + 1;
+    // rows_o may cover several query tokens (rows_o > H): the tiles run to the last
+    // row's causal length, and each row masks past its own
+    const int L = bad ? 0 : seq_len - p.s_q + (row0 + rows_o - 1) / p.H + 1;
     const int tiles = (L + KT - 1) / KT;
     const int jt0 = it.tile_begin;
     const int jt1 = min(it.tile_end, tiles);
@@ -370,6 +372,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
         const int tb = 16 * half;
         const bool row_ok = r < rows_o;
         const int g = row_ok ? ((h0 + r) % p.H) / hpg : 0;
+        const int L_r = bad ? 0 : seq_len - p.s_q + (row0 + (row_ok ? r : 0)) / p.H + 1;   // this row's length
         const float coef = row_ok ? coef_s[r] : 0.f;
         const float rs = p.scale * kLog2e;
         float m_run = -INFINITY, l_run = 0.f;
@@ -386,7 +389,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             tc_fence_after();
             uint8_t* stg = sm + LY::kOffStage + s * LY::kStage;
             const void* ak_t = stg + LY::kSLat + LY::kSRope;
-            const int valid = min(KT, L - tile * KT);
+            const int valid = min(KT, L - tile * KT);          // the CTA's longest row
+            const int valid_r = min(KT, L_r - tile * KT);      // this row (may be <= 0)
             float lg[kQ4][16];
 #pragma unroll
             for (int q = 0; q < kQ4; ++q) {
@@ -402,7 +406,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                     else
                         lg[q][jj] = fmaf(coef * load_alpha<AKH>(ak_t, t * p.G + g), __uint_as_float(sc[jj]),
                                          __uint_as_float(sr[jj]));
-                    if (t >= valid) lg[q][jj] = -INFINITY;
+                    if (t >= valid_r) lg[q][jj] = -INFINITY;
                 }
             }
             tc_fence_before();
@@ -453,6 +457,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                 named_bar_sync();
             }
             l_run *= corr;
+            // a row with no token yet (m_run still -inf) gets P = 0, not exp2(NaN)
+            const float m_e = (m_run == -INFINITY) ? 0.f : m_run;
             // P^T row r, this thread's tokens, into the RoPE slot (bf16)
             uint8_t* pT = stg + LY::kSLat;
             float psum = 0.f;
@@ -461,8 +467,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                 uint32_t w8[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const float e0 = fast_exp2(lg[q][2 * u] - m_run);
-                    const float e1 = fast_exp2(lg[q][2 * u + 1] - m_run);
+                    const float e0 = fast_exp2(lg[q][2 * u] - m_e);
+                    const float e1 = fast_exp2(lg[q][2 * u + 1] - m_e);
                     psum += e0 + e1;
                     const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
                     w8[u] = *reinterpret_cast<const uint32_t*>(&b2);
@@ -818,6 +824,19 @@ bool pair_shape(const qkmla_decode_args* a) {
 // Batches whose split plan every decode CTA computes itself (no scheduler launch).
 bool sched_in_kernel(const qkmla_decode_args* a) { return a->B >= 1 && a->B <= dec::kMaxBSched; }
 
+// Query rows per CTA of the 64-row kernel.  With fewer than 64 heads it packs k
+// query tokens of a sequence (k dividing s_q), so that a CTA streams each tile
+// once for all of them, while k H stays within the 64 MMA rows and within the
+// RoPE slot that P^T reuses (k H rows x tile tokens in bf16 <= d_r columns).
+int tc_rows(const qkmla_decode_args* a) {
+    if (a->H >= 64) return 64;
+    const int cap = a->d_r < 64 ? a->d_r : 64;
+    int rows = a->H;
+    for (int k = 2; k <= a->s_q; ++k)
+        if (a->s_q % k == 0 && a->H * k <= cap && (a->H * k) % 16 == 0) rows = a->H * k;
+    return rows;
+}
+
 // Shapes the tensor-core kernel is built for (bf16 cache).
 bool tc_supported(const qkmla_decode_args* a) {
     if (a->cache_dtype != QKMLA_BF16) return false;
@@ -834,7 +853,7 @@ bool tc_supported(const qkmla_decode_args* a) {
 }
 
 size_t tc_workspace(const qkmla_decode_args* a, int sms, int* max_items_out) {
-    const int rows_o = a->H < 64 ? a->H : 64;
+    const int rows_o = pair_shape(a) ? 64 : tc_rows(a);
     const int n_rb = a->s_q * a->H / rows_o;
     const int target = (sms + n_rb - 1) / n_rb;
     int max_items = a->B + target + 1;
@@ -853,7 +872,7 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     const int sms = device_sm_count();
     int max_items = 0;
     tc_workspace(a, sms, &max_items);
-    const int rows_o = a->H < 64 ? a->H : 64;
+    const int rows_o = pair_shape(a) ? 64 : tc_rows(a);
     const int n_rb = a->s_q * a->H / rows_o;
     uint8_t* ws = (uint8_t*)a->workspace;
     WorkItem* items = (WorkItem*)ws;

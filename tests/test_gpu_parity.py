@@ -373,6 +373,23 @@ def test_decode_split_counts_agree(Q, splits, simt):
     check_close(_np(st.lse), l_auto, "bf16", f"splits={splits} vs auto lse", edge=True)
 
 
+@pytest.mark.parametrize("splits", [0, 2, 3])
+def test_packed_query_tokens_mask_per_row(Q, splits):
+    """The 64-row kernel packs two query tokens of the small shape (16 heads) into
+    one CTA; a sequence of 65 tokens split at the 64-token tile boundary gives the
+    first query token (length 64) no token in the second item, the second query
+    token (length 65) one."""
+    from qk_normed_latent_gb300.pipeline import DeviceState
+    w = W.small(W.WORKLOADS[1], 3, (65, 2, 700), s_q=2, n_append=2)
+    st = DeviceState(w)
+    st.step()
+    st.decode(num_splits=splits)
+    assert_status_ok(Q)
+    o_ref, lse_ref = OR.reference(w)
+    check_close(_np(st.o), o_ref, "bf16", f"packed s_q=2 splits={splits} o", edge=True)
+    check_close(_np(st.lse), lse_ref, "bf16", f"packed s_q=2 splits={splits} lse", edge=True)
+
+
 def test_decode_bad_page_id_is_reported_not_trapped(Q):
     from qk_normed_latent_gb300.pipeline import DeviceState
     w = _workload("dsv3_ragged")
