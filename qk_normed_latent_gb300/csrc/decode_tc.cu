@@ -67,7 +67,12 @@ struct Layout {
     static constexpr int kSLat = kLatBlocks * KT * 128;
     static constexpr int kSRope = KT * kRopeRowBytes;
     static constexpr int kSAk = KT * kMaxG * 4;
-    static constexpr int kStage = ((kSLat + kSRope + kSAk) + 1023) / 1024 * 1024;
+    // P^T (up to 64 rows x KT tokens, bf16) reuses the tile's RoPE slot when it fits
+    // there (d_c = 512); for d_c = 256 it has a slot of its own, so 64 rows fit
+    static constexpr int kPBytes = kRowsMMA * KT * 2;
+    static constexpr bool kPOwn = kPBytes > kSRope;
+    static constexpr int kOffP = kPOwn ? (kSLat + kSRope + kSAk + 1023) / 1024 * 1024 : kSLat;
+    static constexpr int kStage = ((kPOwn ? kOffP + kPBytes : kSLat + kSRope + kSAk) + 1023) / 1024 * 1024;
     static constexpr int kQ = ((kQLat + kQRope) + 1023) / 1024 * 1024;
     static constexpr int kOffQ = 0;
     static constexpr int kOffStage = kQ;
@@ -297,7 +302,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
                 if (!wait_bounded(&pfull[s], (jj / NST) & 1, p.status, p.wait_ns)) return false;
                 tc_fence_after();
                 const uint32_t st_addr = smem_u32(sm + LY::kOffStage + s * LY::kStage);
-                const uint32_t p_addr = st_addr + LY::kSLat;       // P^T lives in the RoPE slot
+                const uint32_t p_addr = st_addr + LY::kOffP;       // P^T: the RoPE slot or its own
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
@@ -460,7 +465,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             // a row with no token yet (m_run still -inf) gets P = 0, not exp2(NaN)
             const float m_e = (m_run == -INFINITY) ? 0.f : m_run;
             // P^T row r, this thread's tokens, into the RoPE slot (bf16)
-            uint8_t* pT = stg + LY::kSLat;
+            uint8_t* pT = stg + LY::kOffP;
             float psum = 0.f;
 #pragma unroll
             for (int q = 0; q < kQ4; ++q) {
@@ -826,11 +831,11 @@ bool sched_in_kernel(const qkmla_decode_args* a) { return a->B >= 1 && a->B <= d
 
 // Query rows per CTA of the 64-row kernel.  With fewer than 64 heads it packs k
 // query tokens of a sequence (k dividing s_q), so that a CTA streams each tile
-// once for all of them, while k H stays within the 64 MMA rows and within the
-// RoPE slot that P^T reuses (k H rows x tile tokens in bf16 <= d_r columns).
+// once for all of them, while k H stays within the 64 MMA rows and, for d_c =
+// 512, within the RoPE slot that P^T reuses there (k H <= d_r).
 int tc_rows(const qkmla_decode_args* a) {
     if (a->H >= 64) return 64;
-    const int cap = a->d_r < 64 ? a->d_r : 64;
+    const int cap = (a->d_c == 256 || a->d_r >= 64) ? 64 : a->d_r;
     int rows = a->H;
     for (int k = 2; k <= a->s_q; ++k)
         if (a->s_q % k == 0 && a->H * k <= cap && (a->H * k) % 16 == 0) rows = a->H * k;
@@ -846,7 +851,7 @@ bool tc_supported(const qkmla_decode_args* a) {
     if (a->page_size % (a->d_c == 256 ? 64 : 32)) return false;
     const int rows_o = a->H < 64 ? a->H : 64;
     if (rows_o % 16 || a->H % rows_o) return false;
-    if (rows_o > a->d_r) return false;     // P^T (rows_o x tile tokens) reuses the tile's RoPE slot
+    if (a->d_c != 256 && rows_o > a->d_r) return false;   // P^T (rows_o x tile tokens) reuses the RoPE slot
     if (((uintptr_t)a->kv_cache % 16) || ((uintptr_t)a->q_tilde % 16) || ((uintptr_t)a->o % 16)) return false;
     if (!(a->flags & QKMLA_FLAG_PLAIN_MLA) && ((uintptr_t)a->ak_cache % 16)) return false;
     return true;
