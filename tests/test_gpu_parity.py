@@ -249,11 +249,15 @@ CASES = {
     "dsv3_sq16_clean": (4, dict(B=2, lens=(16, 3001), kw=dict(s_q=16, n_append=16, outlier_frac=0.0))),
     "small_sq8": (1, dict(B=3, lens=(8, 1000, 4100), kw=dict(s_q=8, n_append=8))),
     "tiny_fp32_sq8": (0, dict(B=2, lens=(9, 256), kw=dict(s_q=8, n_append=8))),
+    # the 64-row kernel with 64 rows at d_c = 256 (P^T in its own stage slot): 64 heads of one
+    # query token, and two query tokens of 32 heads packed into one CTA
+    "small_H64": (1, dict(B=3, lens=(1024, 300, 5000), kw=dict(H=64))),
+    "small_H32_sq2": (1, dict(B=3, lens=(700, 2, 4100), kw=dict(H=32, s_q=2, n_append=2))),
 }
 # sequences of 1-130 tokens (the larger-s_q cases include one of exactly s_q tokens, so its first
 # query token sees one token)
 EDGE = {"dsv3_ragged", "mixed_sq2_ragged", "small_ragged", "small_B160_sched", "dsv3_B136_sched",
-        "dsv3_sq4", "dsv3_sq16", "small_sq8"}
+        "dsv3_sq4", "dsv3_sq16", "small_sq8", "small_H32_sq2"}
 
 
 def make_args_only(Q, w):
