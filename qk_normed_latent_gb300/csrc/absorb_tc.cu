@@ -18,7 +18,15 @@
 // the W_g slice), all in flight at once; the 512 threads then split them into
 // bf16 hi/lo in place (each thread reads its elements, a barrier, then writes
 // the swizzled K-major tiles over the raw bytes: 4 bytes in, 2 x 2 bytes out).
+// The output tile is staged in the drained operand region as 128-byte boxes
+// (128-byte swizzle) of the tile's rows -- nr query rows x the group's hpg heads,
+// one 3-D box {128 B of columns, hpg, nr} -- and written by TMA stores, whole
+// lines instead of each thread's 16-byte pieces; shapes whose heads per group do
+// not divide 128 store directly.
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "decode_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace qkmla {
@@ -67,9 +75,9 @@ struct AbsLayout {
 
 template <int DH, int kN, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
-absorb_tc_kernel(const float* __restrict__ q, const float* __restrict__ gq, const float* __restrict__ gk,
-                 const float* __restrict__ wk, int rows, int H, int G, int d_c, float eps, int plain,
-                 OutT* __restrict__ qt, float* __restrict__ aq, int* status) {
+absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ q, const float* __restrict__ gq,
+                 const float* __restrict__ gk, const float* __restrict__ wk, int rows, int H, int G, int d_c, float eps,
+                 int plain, int tma_out, OutT* __restrict__ qt, float* __restrict__ aq, int* status) {
     using LY = AbsLayout<DH, kN>;
     static_assert(LY::kAIter * kThreads == kM * LY::kG8 && LY::kBIter * kThreads == kN * LY::kG8, "tiling");
     static_assert(32 % LY::kG8 == 0, "a row's groups sit in one warp");
@@ -215,7 +223,9 @@ absorb_tc_kernel(const float* __restrict__ q, const float* __restrict__ gq, cons
     // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (output rows) and
     //      columns kN/4 (w / 4) .. (latent coordinates n0 + ...) ----
     constexpr int kC16 = kN / 64;                  // 16-column chunks per warp
-    if (__all_sync(0xffffffffu, ok)) {
+    constexpr int kBoxCols = 128 / (int)sizeof(OutT);
+    const bool all_ok = __syncthreads_and(ok) != 0;
+    if (all_ok) {
         const int ml = 32 * (warp & 3) + lane;
         const int c_base = (kN / 4) * (warp >> 2);
         const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + c_base;
@@ -223,29 +233,46 @@ absorb_tc_kernel(const float* __restrict__ q, const float* __restrict__ gq, cons
 #pragma unroll
         for (int c = 0; c < kC16; ++c) tmem_ld16(taddr + 16 * c, v[c]);
         tmem_wait_ld();
-        if (ml < m_valid) {
-            const int m = m0 + ml, r = m / hpg, h = g * hpg + m % hpg;
-            OutT* dst = qt + ((size_t)r * H + h) * d_c + n0 + c_base;
+        // this thread's 64 columns as stored (bf16: 128 B, one box row; fp32: 256 B, two)
+        uint32_t w[kC16 * 16 * (int)sizeof(OutT) / 4];
 #pragma unroll
-            for (int c = 0; c < kC16; ++c) {
+        for (int c = 0; c < kC16; ++c) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
                 if constexpr (sizeof(OutT) == 2) {
-                    uint32_t w[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const __nv_bfloat162 b2 =
-                            __floats2bfloat162_rn(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1]));
-                        w[i] = *reinterpret_cast<const uint32_t*>(&b2);
-                    }
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * c);
-                    d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1]));
+                    w[8 * c + i / 2] = *reinterpret_cast<const uint32_t*>(&b2);
                 } else {
-                    float4* d4 = reinterpret_cast<float4*>(dst + 16 * c);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        d4[i] = make_float4(__uint_as_float(v[c][4 * i]), __uint_as_float(v[c][4 * i + 1]),
-                                            __uint_as_float(v[c][4 * i + 2]), __uint_as_float(v[c][4 * i + 3]));
+                    w[16 * c + i] = v[c][i];
+                    w[16 * c + i + 1] = v[c][i + 1];
                 }
+            }
+        }
+        constexpr int kChunks = (int)(sizeof(w) / 16);           // 16-byte chunks of the 64 columns
+        if (tma_out) {
+            // the operand region is drained (every MMA has completed): box c_base / kBoxCols onward
+#pragma unroll
+            for (int q16 = 0; q16 < kChunks; ++q16) {
+                const int col = c_base * (int)sizeof(OutT) / 16 + q16;          // 16-byte chunk of the row
+                uint8_t* box = sm + (col / 8) * (kM * 128) + ml * 128;
+                *reinterpret_cast<uint4*>(box + (((uint32_t)(col & 7) ^ (uint32_t)(ml & 7)) << 4)) =
+                    make_uint4(w[4 * q16], w[4 * q16 + 1], w[4 * q16 + 2], w[4 * q16 + 3]);
+            }
+        } else if (ml < m_valid) {
+            const int m = m0 + ml, r = m / hpg, h = g * hpg + m % hpg;
+            uint4* d4 = reinterpret_cast<uint4*>(qt + ((size_t)r * H + h) * d_c + n0 + c_base);
+#pragma unroll
+            for (int q16 = 0; q16 < kChunks; ++q16) d4[q16] = make_uint4(w[4 * q16], w[4 * q16 + 1], w[4 * q16 + 2], w[4 * q16 + 3]);
+        }
+        if (tma_out) {
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                // rows past the group's rows fall outside the tensor's row range and are not written
+                for (int bx = 0; bx < kN / kBoxCols; ++bx)
+                    tma_store_3d(&tm_out, n0 + bx * kBoxCols, g * hpg, m0 / hpg, sm + bx * (kM * 128));
+                dec::bulk_commit_group();
+                dec::bulk_wait_all();
             }
         }
     }
@@ -258,18 +285,39 @@ absorb_tc_kernel(const float* __restrict__ q, const float* __restrict__ gq, cons
     }
 }
 
+// q~ as a 3-D tensor {d_c, H, rows}: boxes {128 B of columns, hpg heads, 128 / hpg rows}, 128-byte swizzle.
+bool make_qt_map(CUtensorMap* m, const void* qt, int esz, int rows, int H, int d_c, int hpg) {
+    auto fn = dec::encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d_c, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d_c * esz, (cuuint64_t)H * d_c * esz};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / esz), (cuuint32_t)hpg, (cuuint32_t)(kM / hpg)};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(qt),
+              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DH, int kN, typename OutT>
 int launch_n(const float* q, const float* gq, const float* gk, const float* wk, int rows, int H, int G, int d_c,
              float eps, bool plain, void* qt, float* aq, cudaStream_t s) {
     using LY = AbsLayout<DH, kN>;
     static_assert(LY::kBytes <= 232448, "shared memory budget");
+    // the staged output boxes must fit the drained operand region
+    constexpr bool kBoxesFit = kN * (int)sizeof(OutT) / 128 * kM * 128 <= LY::kOffG;
     auto k = absorb_tc_kernel<DH, kN, OutT>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes) != cudaSuccess)
         return QKMLA_ERR_CUDA;
-    const int M = rows * (H / G);
+    const int hpg = H / G;
+    const int M = rows * hpg;
+    // TMA stores when a 128-row tile is whole query rows of the group (hpg divides 128)
+    const int tma_out = (kBoxesFit && kM % hpg == 0 && (uintptr_t)qt % 16 == 0) ? 1 : 0;
+    CUtensorMap tq;
+    memset(&tq, 0, sizeof(tq));
+    if (tma_out && !make_qt_map(&tq, qt, (int)sizeof(OutT), rows, H, d_c, hpg)) return QKMLA_ERR_CUDA;
     dim3 grid((M + kM - 1) / kM, d_c / kN, G);
-    return launch_pdl(k, grid, dim3(kThreads), LY::kBytes, s, q, gq, gk, wk, rows, H, G, d_c, eps, plain ? 1 : 0,
-                      (OutT*)qt, aq, device_status_ptr()) == cudaSuccess
+    return launch_pdl(k, grid, dim3(kThreads), LY::kBytes, s, tq, q, gq, gk, wk, rows, H, G, d_c, eps, plain ? 1 : 0,
+                      tma_out, (OutT*)qt, aq, device_status_ptr()) == cudaSuccess
                ? QKMLA_OK
                : QKMLA_ERR_CUDA;
 }
