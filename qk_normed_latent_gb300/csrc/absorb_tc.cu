@@ -25,6 +25,8 @@
 // not divide 128 store directly.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "decode_common.cuh"
 #include "tc_ptx.cuh"
@@ -285,6 +287,217 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const float* __rest
     }
 }
 
+// Many row tiles per (group, 256-latent half) -- large batches: a persistent CTA
+// keeps its W_g half split in shared memory (bf16 hi + lo, loaded before the
+// dependency wait: no kernel of this library writes W^K) and walks row tiles
+// ci, ci + cpp, ...; per tile it loads the q rows, splits them, issues the 24
+// MMAs and stages the bf16 output for TMA stores in the drained A region.  The
+// W split, redone by every CTA of the one-tile kernel, is paid once per CTA.
+template <int DH>
+__global__ void __launch_bounds__(kThreads, 1)
+absorb_tc_persistent(const __grid_constant__ CUtensorMap tm_out, const float* __restrict__ q,
+                     const float* __restrict__ gq, const float* __restrict__ gk, const float* __restrict__ wk,
+                     int rows, int H, int G, int d_c, float eps, int plain, int cpp,
+                     __nv_bfloat16* __restrict__ qt, float* __restrict__ aq, int* status) {
+    using LY = AbsLayout<DH, kNMax>;
+    static_assert(LY::kA >= kNMax * 2 / 128 * kM * 128, "the bf16 output boxes fit the A region");
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    float* rawA = reinterpret_cast<float*>(sm + LY::kOffA);
+    float* rawB = reinterpret_cast<float*>(sm + LY::kOffB);
+    float* gprod = reinterpret_cast<float*>(sm + LY::kOffG);
+    uint64_t* bar = (uint64_t*)(sm + LY::kOffMisc);                 // [0] W, [1] A of a tile, [2] MMAs of a tile
+    uint32_t* tmem_slot = (uint32_t*)(bar + 4);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int NH = d_c / kNMax;
+    const int pr = blockIdx.x % (G * NH), ci = blockIdx.x / (G * NH);
+    const int g = pr / NH, nh = pr % NH, n0 = nh * kNMax;
+    const int hpg = H / G;
+    const int M = rows * hpg;
+    const int n_tiles = (M + kM - 1) / kM;
+
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
+        fence_barrier_init();
+        prefetch_tmap(&tm_out);
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kNMax);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    // ---- W_g rows n0 .. n0 + 255: before the dependency wait ----
+    if (tid == 0) mbar_arrive_expect_tx(&bar[0], (uint32_t)LY::kB);
+    if (tid < LY::kBCopies) {
+        constexpr int bytes = LY::kB / LY::kBCopies;
+        bulk_load(reinterpret_cast<uint8_t*>(rawB) + tid * bytes,
+                  reinterpret_cast<const uint8_t*>(wk + ((size_t)g * d_c + n0) * DH) + tid * bytes, bytes, &bar[0]);
+    }
+    if (tid < DH) gprod[tid] = plain ? 1.f : gq[tid] * gk[tid];
+    bool ok = mbar_wait(&bar[0], 0, 1u << 24);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) report(status, QKMLA_ERR_TIMEOUT);
+        mbar_wait(&bar[0], 0, 1u << 24);       // copies still in flight land before the memory is released
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(*tmem_slot, kNMax);
+        return;
+    }
+    {
+        float x[LY::kBIter][8];
+#pragma unroll
+        for (int i = 0; i < LY::kBIter; ++i) {
+            const int e = tid + i * kThreads;
+            const int nl = e / LY::kG8, k8 = e % LY::kG8;
+            const float4 v0 = *reinterpret_cast<const float4*>(rawB + nl * DH + k8 * 8);
+            const float4 v1 = *reinterpret_cast<const float4*>(rawB + nl * DH + k8 * 8 + 4);
+            x[i][0] = v0.x; x[i][1] = v0.y; x[i][2] = v0.z; x[i][3] = v0.w;
+            x[i][4] = v1.x; x[i][5] = v1.y; x[i][6] = v1.z; x[i][7] = v1.w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < LY::kBIter; ++i) {
+            const int e = tid + i * kThreads;
+            const int nl = e / LY::kG8, k8 = e % LY::kG8;
+            const uint32_t off = (k8 >> 3) * (kNMax * 128) + sw128_offset(nl, (k8 & 7) * 8);
+            split_store(sm + LY::kOffB, sm + LY::kOffBlo, off, x[i]);
+        }
+    }
+    pdl_wait();                // q comes from an earlier kernel; q~ is written below
+    pdl_trigger();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    int it = 0;
+    for (int t = ci; t < n_tiles && ok; t += cpp, ++it) {
+        const int m0 = t * kM, m_valid = min(kM, M - m0);
+        // ---- this tile's q rows (the previous tile's output boxes have been read out) ----
+        if (tid == 0) mbar_arrive_expect_tx(&bar[1], (uint32_t)(m_valid * DH * 4));
+        __syncwarp();
+        if (tid < m_valid) {
+            const int m = m0 + tid, r = m / hpg, h = g * hpg + m % hpg;
+            bulk_load(rawA + tid * DH, q + ((size_t)r * H + h) * DH, DH * 4, &bar[1]);
+        }
+        ok = mbar_wait(&bar[1], it & 1, 1u << 24);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) report(status, QKMLA_ERR_TIMEOUT);
+            mbar_wait(&bar[1], it & 1, 1u << 24);
+            ok = false;
+            break;
+        }
+        // ---- A = q * gamma_q * gamma_k, split hi/lo in place; alpha^q from the raw q (first half only) ----
+        {
+            float x[LY::kAIter][8];
+#pragma unroll
+            for (int i = 0; i < LY::kAIter; ++i) {
+                const int e = tid + i * kThreads;
+                const int ml = e / LY::kG8, k8 = e % LY::kG8;
+                if (ml < m_valid) {
+                    const float4 v0 = *reinterpret_cast<const float4*>(rawA + ml * DH + k8 * 8);
+                    const float4 v1 = *reinterpret_cast<const float4*>(rawA + ml * DH + k8 * 8 + 4);
+                    x[i][0] = v0.x; x[i][1] = v0.y; x[i][2] = v0.z; x[i][3] = v0.w;
+                    x[i][4] = v1.x; x[i][5] = v1.y; x[i][6] = v1.z; x[i][7] = v1.w;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) x[i][u] = 0.f;
+                }
+                if (nh == 0) {
+                    float ss = 0.f;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) ss = fmaf(x[i][u], x[i][u], ss);
+#pragma unroll
+                    for (int o = LY::kG8 / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                    if (k8 == 0 && ml < m_valid) {
+                        const int m = m0 + ml, r = m / hpg, h = g * hpg + m % hpg;
+                        aq[(size_t)r * H + h] = plain ? 1.f : 1.f / sqrtf(ss / (float)DH + eps);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[i][u] *= gprod[k8 * 8 + u];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < LY::kAIter; ++i) {
+                const int e = tid + i * kThreads;
+                const int ml = e / LY::kG8, k8 = e % LY::kG8;
+                const uint32_t off = (k8 >> 3) * (kM * 128) + sw128_offset(ml, (k8 & 7) * 8);
+                split_store(sm + LY::kOffA, sm + LY::kOffAlo, off, x[i]);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            const uint32_t idesc = idesc_bf16(kM, kNMax, 0, 0);
+            const uint32_t a_hi = smem_u32(sm + LY::kOffA), a_lo = smem_u32(sm + LY::kOffAlo);
+            const uint32_t b_hi = smem_u32(sm + LY::kOffB), b_lo = smem_u32(sm + LY::kOffBlo);
+#pragma unroll
+            for (int kb = 0; kb < DH / 16; ++kb) {
+                const uint32_t ao = (kb >> 2) * (kM * 128) + (kb & 3) * 32;
+                const uint32_t bo = (kb >> 2) * (kNMax * 128) + (kb & 3) * 32;
+                mma_bf16(tmem, smem_desc(a_hi + ao, 16, 1024, kSwizzle128B), smem_desc(b_hi + bo, 16, 1024, kSwizzle128B),
+                         idesc, kb > 0 ? 1u : 0u);
+                mma_bf16(tmem, smem_desc(a_hi + ao, 16, 1024, kSwizzle128B), smem_desc(b_lo + bo, 16, 1024, kSwizzle128B),
+                         idesc, 1u);
+                mma_bf16(tmem, smem_desc(a_lo + ao, 16, 1024, kSwizzle128B), smem_desc(b_hi + bo, 16, 1024, kSwizzle128B),
+                         idesc, 1u);
+            }
+            mma_commit(&bar[2]);
+        }
+        __syncwarp();
+        ok = mbar_wait(&bar[2], it & 1, 1u << 24);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) report(status, QKMLA_ERR_TIMEOUT);
+            mbar_wait(&bar[2], it & 1, 1u << 24);   // the MMAs finish before TMEM is released
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        // ---- epilogue: TMEM -> bf16 boxes in the drained A region -> TMA stores ----
+        {
+            constexpr int kC16 = kNMax / 64;
+            const int ml = 32 * (warp & 3) + lane;
+            const int c_base = (kNMax / 4) * (warp >> 2);
+            const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + c_base;
+            uint32_t v[kC16][16];
+#pragma unroll
+            for (int c = 0; c < kC16; ++c) tmem_ld16(taddr + 16 * c, v[c]);
+            tmem_wait_ld();
+            uint32_t w[kC16 * 8];
+#pragma unroll
+            for (int c = 0; c < kC16; ++c)
+#pragma unroll
+                for (int i = 0; i < 16; i += 2) {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1]));
+                    w[8 * c + i / 2] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+            uint8_t* box = sm + (c_base / 64) * (kM * 128) + ml * 128;     // 64 bf16 columns = one box row
+#pragma unroll
+            for (int q16 = 0; q16 < 8; ++q16)
+                *reinterpret_cast<uint4*>(box + (((uint32_t)q16 ^ (uint32_t)(ml & 7)) << 4)) =
+                    make_uint4(w[4 * q16], w[4 * q16 + 1], w[4 * q16 + 2], w[4 * q16 + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            // rows past the group's rows fall outside the tensor's row range and are not written
+            for (int bx = 0; bx < kNMax / 64; ++bx)
+                tma_store_3d(&tm_out, n0 + bx * 64, g * hpg, m0 / hpg, sm + bx * (kM * 128));
+            dec::bulk_commit_group();
+            dec::bulk_wait_read_all();          // the boxes are read out before the next q rows land
+        }
+        __syncthreads();
+    }
+    if (tid == 0) dec::bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kNMax);
+    }
+}
+
 // q~ as a 3-D tensor {d_c, H, rows}: boxes {128 B of columns, hpg heads, 128 / hpg rows}, 128-byte swizzle.
 bool make_qt_map(CUtensorMap* m, const void* qt, int esz, int rows, int H, int d_c, int hpg) {
     auto fn = dec::encode_fn();
@@ -322,12 +535,38 @@ int launch_n(const float* q, const float* gq, const float* gk, const float* wk, 
                : QKMLA_ERR_CUDA;
 }
 
+// Persistent CTAs keeping a W_g half resident (d_h = 128, bf16 q~, enough row tiles
+// per (group, half) for the W split to pay off): cpp CTAs per (group, half).
+int launch_persistent(const float* q, const float* gq, const float* gk, const float* wk, int rows, int H, int G,
+                      int d_c, float eps, bool plain, void* qt, float* aq, int cpp, cudaStream_t s) {
+    using LY = AbsLayout<128, kNMax>;
+    auto k = absorb_tc_persistent<128>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kBytes) != cudaSuccess)
+        return QKMLA_ERR_CUDA;
+    CUtensorMap tq;
+    if (!make_qt_map(&tq, qt, 2, rows, H, d_c, H / G)) return QKMLA_ERR_CUDA;
+    dim3 grid(cpp * G * (d_c / kNMax));
+    return launch_pdl(k, grid, dim3(kThreads), LY::kBytes, s, tq, q, gq, gk, wk, rows, H, G, d_c, eps, plain ? 1 : 0,
+                      cpp, (__nv_bfloat16*)qt, aq, device_status_ptr()) == cudaSuccess
+               ? QKMLA_OK
+               : QKMLA_ERR_CUDA;
+}
+
 // 256-latent tiles, or 64-latent ones when the 256-wide grid has fewer than 64 CTAs.
 template <int DH, typename OutT>
 int launch_t(const float* q, const float* gq, const float* gk, const float* wk, int rows, int H, int G, int d_c,
              float eps, bool plain, void* qt, float* aq, cudaStream_t s) {
     const int M = rows * (H / G);
-    const int ctas_wide = ((M + kM - 1) / kM) * (d_c / kNMax) * G;
+    const int hpg = H / G;
+    const int pairs = G * (d_c / kNMax);
+    const int n_tiles = (M + kM - 1) / kM;
+    if constexpr (DH == 128 && sizeof(OutT) == 2) {
+        // at least two tiles per persistent CTA when every SM gets one
+        const int cpp = std::max(1, device_sm_count() / pairs);
+        if (kM % hpg == 0 && (uintptr_t)qt % 16 == 0 && pairs <= device_sm_count() && n_tiles >= 2 * cpp)
+            return launch_persistent(q, gq, gk, wk, rows, H, G, d_c, eps, plain, qt, aq, cpp, s);
+    }
+    const int ctas_wide = n_tiles * (d_c / kNMax) * G;
     return ctas_wide < 64 ? launch_n<DH, 64, OutT>(q, gq, gk, wk, rows, H, G, d_c, eps, plain, qt, aq, s)
                           : launch_n<DH, kNMax, OutT>(q, gq, gk, wk, rows, H, G, d_c, eps, plain, qt, aq, s);
 }
