@@ -137,8 +137,9 @@ append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r
         for (int t = 0; t < nvalid; ++t)
             bulk_load(Cs + t * kKS, c_new + (int64_t)(n0 + t) * kDc + k0, (uint32_t)(kKS * 4), bar);
     }
-    // thread (t, q): token t = tid / 16, columns / elements q + 16 v.  What the tail
-    // needs from global memory is loaded now, while the bulk copies are in flight.
+    // The tail's mapping: thread (t, q) owns token t = tid / 16 and columns / elements
+    // q + 16 v.  What the tail needs from global memory is loaded now, while the bulk
+    // copies are in flight.
     const int t = tid >> 4, q = tid & 15;
     const bool tok = t < nvalid;
     const int64_t slot = tok ? slots[n0 + t] : -1;
@@ -150,37 +151,70 @@ append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r
         rv[v] = (rope_here && j < d_r) ? r_new[(int64_t)(n0 + t) * d_r + j] : 0.f;
         gv[v] = (rope_here && j < d_r && !plain && grk != nullptr) ? grk[j] : 1.f;
     }
-    // the statistic is taken over the STORED latent: round the slice to the cache type in place
+    // The statistic is taken over the STORED latent: the slice is rounded to the cache
+    // type and transposed to CsT[k][t] (in the partial-key buffer, unused until the
+    // reduction), so that one 16-byte load gives four tokens of row k.
+    float* CsT = red;
+    static_assert(kKS * kFT <= kFT * kDh, "the transposed slice fits the partial-key buffer");
     const bool ok = mbar_wait(bar, 0, 1u << 24);
     if (ok) {
-        for (int e = tid; e < kFT * kKS; e += kThreads) Cs[e] = (e < nvalid * kKS) ? Elem<CT>::cast(Cs[e]) : 0.f;
+        for (int e = tid; e < kFT * kKS; e += kThreads) {
+            const int tt = e / kKS, k = e % kKS;
+            CsT[k * kFT + tt] = (tt < nvalid) ? Elem<CT>::cast(Cs[e]) : 0.f;
+        }
     } else {
         report(status, QKMLA_ERR_TIMEOUT);
         mbar_wait(bar, 0, 1u << 24);       // copies still in flight land before the CTA's memory is released
     }
     const bool all_ok = __syncthreads_and(ok) != 0;
-    // partial keys over this CTA's rows, one fmaf chain per element over ascending k
-    float acc[U];
+    // Partial keys: thread (part, c) owns key column c for all kFT tokens over rows
+    // [part kRP, part kRP + kRP) of this CTA's slice (a warp reads 32 consecutive W
+    // columns and broadcasts the token values), one fmaf chain per part over
+    // ascending k; the parts are then added in order.
+    constexpr int kParts = kThreads / kDh, kRP = kKS / kParts;
+    static_assert(kThreads % kDh == 0 && kKS % kParts == 0, "thread split of the slice");
+    const int c = tid % kDh, part = tid / kDh;
+    float acc[kFT];
 #pragma unroll
-    for (int u = 0; u < U; ++u) acc[u] = 0.f;
+    for (int i = 0; i < kFT; ++i) acc[i] = 0.f;
     if (all_ok) {
-        const float* cr = Cs + t * kKS;
 #pragma unroll 4
-        for (int k = 0; k < kKS; ++k) {
-            const float a = cr[k];
+        for (int k = part * kRP; k < part * kRP + kRP; ++k) {
+            const float wv = Ws[k * kDh + c];
+            const float4* cp = reinterpret_cast<const float4*>(CsT + k * kFT);
 #pragma unroll
-            for (int u = 0; u < U; ++u) acc[u] = fmaf(a, Ws[k * kDh + q + 16 * u], acc[u]);
+            for (int i4 = 0; i4 < kFT / 4; ++i4) {
+                const float4 cv = cp[i4];
+                acc[4 * i4 + 0] = fmaf(cv.x, wv, acc[4 * i4 + 0]);
+                acc[4 * i4 + 1] = fmaf(cv.y, wv, acc[4 * i4 + 1]);
+                acc[4 * i4 + 2] = fmaf(cv.z, wv, acc[4 * i4 + 2]);
+                acc[4 * i4 + 3] = fmaf(cv.w, wv, acc[4 * i4 + 3]);
+            }
         }
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) red[t * kDh + q + 16 * u] = acc[u];
     pdl_wait();                            // the cache writes follow the previous kernel
     const bool slot_ok = tok && slot >= 0 && slot < num_slots;
     // g = 0: this CTA's slice of the token's latent (a pure cast)
     if (g == 0 && all_ok && slot_ok) {
         CT* dst = kv + slot * (int64_t)(kDc + d_r) + k0;
 #pragma unroll
-        for (int v = 0; v < kKS / 16; ++v) Elem<CT>::store(dst + q + 16 * v, Cs[t * kKS + q + 16 * v]);
+        for (int v = 0; v < kKS / 16; ++v) Elem<CT>::store(dst + q + 16 * v, CsT[(q + 16 * v) * kFT + t]);
+    }
+    __syncthreads();                       // Ws and CsT are read: parts 1.. park their sums in Ws
+    float* parked = Ws;                    // [kParts - 1][kFT][kDh]
+    static_assert((kParts - 1) * kFT <= kKS, "the parked sums fit the W slice");
+    if (part > 0) {
+#pragma unroll
+        for (int i = 0; i < kFT; ++i) parked[((part - 1) * kFT + i) * kDh + c] = acc[i];
+    }
+    __syncthreads();
+    if (part == 0) {
+#pragma unroll
+        for (int i = 0; i < kFT; ++i) {
+            float k = acc[i];
+            for (int pp = 1; pp < kParts; ++pp) k += parked[((pp - 1) * kFT + i) * kDh + c];
+            red[i * kDh + c] = k;
+        }
     }
     cluster_sync_all();                    // every CTA's partial keys are in its shared memory
     if (rank == 0) {

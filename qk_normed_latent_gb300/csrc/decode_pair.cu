@@ -163,23 +163,30 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
         const int st = tid - 64;
         if (st < kR) {   // one thread per row: RMS over all 64 RoPE dims, keep this CTA's 32
             const int r = st;
+            // every global read of the prologue is issued before the first shared-memory
+            // store (a load after a store through generic pointers waits for it)
             const float* src = p.qr + (qrow0 + r) * kDR;
+            float v[kDR], gq[kHalfRope];
+#pragma unroll
+            for (int j = 0; j < kDR; ++j) v[j] = src[j];
+#pragma unroll
+            for (int j = 0; j < kHalfRope; ++j) gq[j] = (PLAIN || !p.grq) ? 1.f : p.grq[rank * kHalfRope + j];
+            const float a = PLAIN ? 0.f : p.aq[qrow0 + r];
             float ss = 0.f;
-#pragma unroll 8
-            for (int j = 0; j < kDR; ++j) ss = fmaf(src[j], src[j], ss);
+#pragma unroll
+            for (int j = 0; j < kDR; ++j) ss = fmaf(v[j], v[j], ss);
             // QK mode: scale*log2e rides on the RoPE query, so its MMA output is
             // already the RoPE logit in the exp2 domain
             const float beta = PLAIN ? 1.f : p.scale * kLog2e / sqrtf(ss / (float)kDR + p.eps);
             uint8_t* qrope = sQ + kQLat;
 #pragma unroll
             for (int j = 0; j < kHalfRope; j += 2) {
-                const int c = rank * kHalfRope + j;
-                const float g0 = (PLAIN || !p.grq) ? 1.f : p.grq[c];
-                const float g1 = (PLAIN || !p.grq) ? 1.f : p.grq[c + 1];
-                const __nv_bfloat162 v = __floats2bfloat162_rn(src[c] * g0 * beta, src[c + 1] * g1 * beta);
-                *reinterpret_cast<__nv_bfloat162*>(qrope + sw64_offset(r, j)) = v;
+                const float v0 = rank ? v[kHalfRope + j] : v[j];          // register indices stay static
+                const float v1 = rank ? v[kHalfRope + j + 1] : v[j + 1];
+                const __nv_bfloat162 w2 = __floats2bfloat162_rn(v0 * gq[j] * beta, v1 * gq[j + 1] * beta);
+                *reinterpret_cast<__nv_bfloat162*>(qrope + sw64_offset(r, j)) = w2;
             }
-            coef_s[r] = PLAIN ? 0.f : p.scale * p.aq[qrow0 + r] * kLog2e;
+            coef_s[r] = PLAIN ? 0.f : p.scale * a * kLog2e;
         }
         fence_proxy_async_smem();
     }
@@ -356,15 +363,16 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                             tmem_ld16(tmem + kCSr + lane_base + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(sr + 16 * c));
                     }
                     tmem_wait_ld();
+                    // S is in registers: release it to the next logit MMA before scaling
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sfree);
 #pragma unroll
                     for (int t = 0; t < kT; ++t)
                         pv[t] = PLAIN ? rs * __uint_as_float(sc[t])
                                       : fmaf(coef * load_alpha<AKH>(ak_t, t * p.G + g), __uint_as_float(sc[t]),
                                              __uint_as_float(sr[PLAIN ? 0 : t]));
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sfree);
                 if (valid < kT) {
 #pragma unroll
                     for (int t = 0; t < kT; ++t)

@@ -238,14 +238,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
         // RoPE query: two threads per row
         {
             const int r = st >> 1, half = st & 1;
-            float ss = 0.f;
-            float vals[DR / 2];
+            // every global read of the prologue is issued before the first shared-memory
+            // store: a load after a store through generic pointers waits for it, which
+            // would put one memory round trip per store on this path
+            float vals[DR / 2], gq[DR / 2];
             const float* src = p.qr + (qrow0 + r) * DR + half * (DR / 2);
 #pragma unroll
             for (int j = 0; j < DR / 2; ++j) {
                 vals[j] = (r < rows_o) ? src[j] : 0.f;
-                ss = fmaf(vals[j], vals[j], ss);
+                gq[j] = (PLAIN || !p.grq) ? 1.f : p.grq[half * (DR / 2) + j];
             }
+            const float a = (PLAIN || r >= rows_o || half) ? 1.f : p.aq[qrow0 + r];
+            float ss = 0.f;
+#pragma unroll
+            for (int j = 0; j < DR / 2; ++j) ss = fmaf(vals[j], vals[j], ss);
             ss += __shfl_xor_sync(0xffffffffu, ss, 1);
             // QK mode: the RoPE query carries scale*log2e, so the MMA delivers the RoPE
             // logit already in the exp2 domain
@@ -254,16 +260,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
 #pragma unroll
             for (int j = 0; j < DR / 2; j += 2) {
                 const int c = half * (DR / 2) + j;
-                const float g0 = (PLAIN || !p.grq) ? 1.f : p.grq[c];
-                const float g1 = (PLAIN || !p.grq) ? 1.f : p.grq[c + 1];
-                __nv_bfloat162 v = __floats2bfloat162_rn(vals[j] * g0 * beta, vals[j + 1] * g1 * beta);
+                __nv_bfloat162 v = __floats2bfloat162_rn(vals[j] * gq[j] * beta, vals[j + 1] * gq[j + 1] * beta);
                 const uint32_t off = (DR == 64) ? sw128_offset(r, c) : sw64_offset(r, c);
                 *reinterpret_cast<__nv_bfloat162*>(qrope + off) = v;
             }
-            if (half == 0) {
-                const float a = (PLAIN || r >= rows_o) ? 1.f : p.aq[qrow0 + r];
-                coef_s[r] = p.scale * a * kLog2e;
-            }
+            if (half == 0) coef_s[r] = p.scale * a * kLog2e;
         }
         fence_proxy_async_smem();
     }
@@ -396,27 +397,41 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             const void* ak_t = stg + LY::kSLat + LY::kSRope;
             const int valid = min(KT, L - tile * KT);          // the CTA's longest row
             const int valid_r = min(KT, L_r - tile * KT);      // this row (may be <= 0)
+            // the column scales of this thread's tokens first (shared memory, landed with
+            // the tile the completed logit MMA read), then every TMEM load of the tile and one
+            // wait: the latencies overlap instead of adding up per 32-token chunk
+            float ca[kQ4][16];
+            if (!PLAIN) {
+#pragma unroll
+                for (int q = 0; q < kQ4; ++q)
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        ca[q][jj] = coef * load_alpha<AKH>(ak_t, (32 * q + tb + jj) * p.G + g);
+            }
+            uint32_t sc[kQ4][16], sr[kQ4][16];
+#pragma unroll
+            for (int q = 0; q < kQ4; ++q) {
+                tmem_ld16x2(tmem + LY::kColSc + sb * KT + 32 * q + lane_base, sc[q]);
+                if (!PLAIN) tmem_ld16x2(tmem + LY::kColSr + sb * KT + 32 * q + lane_base, sr[q]);
+            }
+            tmem_wait_ld();
+            // S is in registers: release the buffer to the logit MMA before scaling
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sfree[sb]);
             float lg[kQ4][16];
 #pragma unroll
             for (int q = 0; q < kQ4; ++q) {
-                uint32_t sc[16], sr[16];
-                tmem_ld16x2(tmem + LY::kColSc + sb * KT + 32 * q + lane_base, sc);
-                if (!PLAIN) tmem_ld16x2(tmem + LY::kColSr + sb * KT + 32 * q + lane_base, sr);
-                tmem_wait_ld();
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     const int t = 32 * q + tb + jj;
                     if (PLAIN)
-                        lg[q][jj] = rs * __uint_as_float(sc[jj]);
+                        lg[q][jj] = rs * __uint_as_float(sc[q][jj]);
                     else
-                        lg[q][jj] = fmaf(coef * load_alpha<AKH>(ak_t, t * p.G + g), __uint_as_float(sc[jj]),
-                                         __uint_as_float(sr[jj]));
+                        lg[q][jj] = fmaf(ca[q][jj], __uint_as_float(sc[q][jj]), __uint_as_float(sr[q][jj]));
                     if (t >= valid_r) lg[q][jj] = -INFINITY;
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sfree[sb]);
             float mt = -INFINITY;
 #pragma unroll
             for (int q = 0; q < kQ4; ++q)
