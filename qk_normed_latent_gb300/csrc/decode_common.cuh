@@ -53,6 +53,7 @@ struct TcParams {
     int* status;
     uint64_t wait_ns;          // bound on any single wait (64-row kernel)
     int withhold_tile;         // test hook (64-row kernel): the producer issues no tile from this one on; -1 off
+    uint32_t zero;             // always 0, unknown to the compiler: masks data dependencies into addresses
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -159,14 +160,21 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Wait until every committed bulk copy has completed (its writes performed).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// Relaxed remote arrive: only orders this thread's earlier READS of the rows the
-// other CTA will overwrite (their values are already consumed), no release fence.
-// `dep` is a value computed from every read that must complete first; taking it
-// as an operand makes the instruction wait for those reads.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar, float dep) {
-    asm volatile("{\n\t.reg .f32 d;\n\tmov.f32 d, %1;\n\t"
-                 "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n\t}"
-                 ::"r"(remote_bar), "f"(dep) : "memory");
+// Remote arrive ordered after this thread's earlier READS of the rows the other
+// CTA will overwrite, without a release fence (a release at cluster scope costs
+// ~10 % of the pair kernel).  `dep` is computed from every value those reads
+// returned; masked with `zero` (a kernel argument that is always 0, so no
+// compiler pass can drop it) and added to the barrier address, it makes the
+// arrive's own operand depend on every read: the arrive cannot issue before
+// they have returned their values, after which a remote write cannot change them.
+// (An operand the arrive does not consume is dead code to the assembler, which
+// then may issue the arrive ahead of the reads.)
+__device__ __forceinline__ void mbar_arrive_remote_after(uint32_t remote_bar, uint32_t dep, uint32_t zero) {
+    asm volatile("{\n\t.reg .b32 t, a;\n\t"
+                 "and.b32 t, %1, %2;\n\t"
+                 "add.u32 a, %0, t;\n\t"
+                 "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [a];\n\t}"
+                 ::"r"(remote_bar), "r"(dep), "r"(zero) : "memory");
 }
 // Cluster-wide barrier (all threads of every CTA of the cluster).  The
 // non-aligned form: callers may arrive from diverged code paths.

@@ -354,14 +354,10 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 tc_fence_after();
                 const void* ak_t = sm + kOffStage + s * kStageB + kSLat + kSRope;
                 {
-                    // every load first, one wait: a single TMEM round trip per tile
-                    uint32_t sc[kT], sr[PLAIN ? 1 : kT];
-#pragma unroll
-                    for (int c = 0; c < kT / 16; ++c) {
-                        tmem_ld16(tmem + kCSc + lane_base + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(sc + 16 * c));
-                        if (!PLAIN)
-                            tmem_ld16(tmem + kCSr + lane_base + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(sr + 16 * c));
-                    }
+                    // both loads first (a whole row each), one wait: a single TMEM round trip per tile
+                    uint32_t sc[kT], sr[kT];
+                    tmem_ld64(tmem + kCSc + lane_base, sc);
+                    if (!PLAIN) tmem_ld64(tmem + kCSr + lane_base, sr);
                     tmem_wait_ld();
                     // S is in registers: release it to the next logit MMA before scaling
                     tc_fence_before();
@@ -371,7 +367,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                     for (int t = 0; t < kT; ++t)
                         pv[t] = PLAIN ? rs * __uint_as_float(sc[t])
                                       : fmaf(coef * load_alpha<AKH>(ak_t, t * p.G + g), __uint_as_float(sc[t]),
-                                             __uint_as_float(sr[PLAIN ? 0 : t]));
+                                             __uint_as_float(sr[t]));
                 }
                 if (valid < kT) {
 #pragma unroll
@@ -482,7 +478,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                     const uint32_t xdep_w = __reduce_xor_sync(0xffffffffu, xdep);
                     if (lane == 0 && j + 1 < n_t) {
                         mbar_arrive_expect_tx(&xfull[sub], kXSlice);
-                        mbar_arrive_remote_relaxed(peer_xfree, __uint_as_float(xdep_w));
+                        mbar_arrive_remote_after(peer_xfree, xdep_w, p.zero);
                     }
                 }
                 // own max + partner max bounds the tile max: when it cannot move the running

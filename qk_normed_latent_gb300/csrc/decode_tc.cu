@@ -967,6 +967,7 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
     const bool stall = (a->flags & QKMLA_FLAG_TEST_STALL) != 0;
     tp.wait_ns = stall ? 1000000ull : kWaitNs;
     tp.withhold_tile = stall ? 1 : -1;
+    tp.zero = 0;
     const bool plain = (a->flags & QKMLA_FLAG_PLAIN_MLA) != 0;
     const bool akh = !plain && (a->flags & QKMLA_FLAG_ALPHA_F16) != 0;
     int rc;

@@ -1,0 +1,47 @@
+"""The decode call is deterministic: repeated calls on the same inputs give the
+same bits.  Every reduction in the kernels runs in a fixed order (the exchange
+of partial logits between the two CTAs of a pair, the split-KV combine), so a
+difference between two calls can only come from a read racing a write -- e.g.
+a CTA overwriting the rows its partner is still reading.  Such a race shows as
+rare, small differences, which parity tolerances would hide; comparing bits
+over many calls exposes it.  The long-context workload (four 256k-token
+sequences, split over every CTA pair, thousands of tiles per pair) keeps the
+exchange running longest; the small one exercises the 64-row kernel."""
+import hashlib
+
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def Q():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from qk_normed_latent_gb300 import build as B
+    B.build()
+    import qk_normed_latent_gb300 as Q
+    return Q
+
+
+@pytest.mark.parametrize("widx,repeats", [(3, 40), (2, 20), (1, 40)])
+def test_decode_repeats_bit_identical(Q, widx, repeats):
+    from qk_normed_latent_gb300.pipeline import DeviceState
+    st = DeviceState(W.WORKLOADS[widx], sentinel=False)
+    for _ in range(2):
+        st.step()
+    torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")   # cold L2 before every call
+    digests = []
+    for k in range(repeats):
+        flush.fill_(k & 255)
+        st.decode()
+        torch.cuda.synchronize()
+        assert Q.get_device_status() == 0
+        h = hashlib.sha1(st.o.view(torch.uint8).cpu().numpy().tobytes())
+        h.update(st.lse.view(torch.uint8).cpu().numpy().tobytes())
+        digests.append(h.hexdigest())
+    assert len(set(digests)) == 1, f"{len(set(digests))} distinct outputs over {repeats} calls"
