@@ -378,12 +378,11 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 bool ok_a = got_s;
                 if (j >= 1) ok_a = __all_sync(0xffffffffu, wait_bounded(ownfree, (j - 1) & 1, p.status)) && ok_a;
                 tc_fence_after();
+                {
+                    uint32_t w64[kT];
 #pragma unroll
-                for (int q = 0; q < kT / 16; ++q) {
-                    uint32_t w16[16];
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) w16[jj] = __float_as_uint(pv[16 * q + jj]);
-                    tmem_st16(tmem + kCOwn + lane_base + 16 * q, w16);
+                    for (int t = 0; t < kT; ++t) w64[t] = __float_as_uint(pv[t]);
+                    tmem_st64(tmem + kCOwn + lane_base, w64);
                 }
                 tmem_wait_st();
                 // stage fp16 relative to the row max, once the previous send has read Y
@@ -441,9 +440,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 tc_fence_after();
                 {
                     uint32_t v[kT];
-#pragma unroll
-                    for (int q = 0; q < kT / 16; ++q)
-                        tmem_ld16(tmem + kCOwn + lane_base + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(v + 16 * q));
+                    tmem_ld64(tmem + kCOwn + lane_base, v);
                     tmem_wait_ld();
 #pragma unroll
                     for (int t = 0; t < kT; ++t) lg[t] = __uint_as_float(v[t]);
@@ -601,36 +598,40 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                                   ? p.o_part + ((size_t)it.part * p.s_q * p.H + (size_t)qi * p.H + r) * kDC + rank * kHalfLat
                                   : nullptr;
 #pragma unroll 1
-            for (int c16 = 0; c16 < kHalfLat; c16 += 16) {
-                uint32_t v[16];
+            for (int c64 = 0; c64 < kHalfLat; c64 += 64) {
+                uint32_t v[64];
                 if (n_t > 0 && got_last) {
-                    tmem_ld16(tmem + kCO + c16 + lane_base, v);
+                    tmem_ld64(tmem + kCO + c64 + lane_base, v);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) v[jj] = 0u;
+                    for (int jj = 0; jj < 64; ++jj) v[jj] = 0u;
                 }
-                float o16[16];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) o16[jj] = __uint_as_float(v[jj]) * inv;
-                if (dst_part) {
-                    float4* d4 = reinterpret_cast<float4*>(dst_part + c16);
+                for (int c16 = 0; c16 < 64; c16 += 16) {
+                    float o16[16];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) d4[q] = make_float4(o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
-                } else if (p.o_dtype == QKMLA_F32) {
-                    float4* d4 = reinterpret_cast<float4*>((float*)p.o + orow * kDC + rank * kHalfLat + c16);
+                    for (int jj = 0; jj < 16; ++jj) o16[jj] = __uint_as_float(v[c16 + jj]) * inv;
+                    const int col = rank * kHalfLat + c64 + c16;
+                    if (dst_part) {
+                        float4* d4 = reinterpret_cast<float4*>(dst_part + c64 + c16);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) d4[q] = make_float4(o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
-                } else {
-                    uint32_t w[8];
+                        for (int q = 0; q < 4; ++q) d4[q] = make_float4(o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
+                    } else if (p.o_dtype == QKMLA_F32) {
+                        float4* d4 = reinterpret_cast<float4*>((float*)p.o + orow * kDC + col);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(o16[2 * q], o16[2 * q + 1]);
-                        w[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                        for (int q = 0; q < 4; ++q) d4[q] = make_float4(o16[4 * q], o16[4 * q + 1], o16[4 * q + 2], o16[4 * q + 3]);
+                    } else {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(o16[2 * q], o16[2 * q + 1]);
+                            w[q] = *reinterpret_cast<const uint32_t*>(&b2);
+                        }
+                        uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)p.o + orow * kDC + col);
+                        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
                     }
-                    uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)p.o + orow * kDC + rank * kHalfLat + c16);
-                    d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
         }
