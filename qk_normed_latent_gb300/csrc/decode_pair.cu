@@ -363,11 +363,22 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(sfree);
+                    if (PLAIN) {
 #pragma unroll
-                    for (int t = 0; t < kT; ++t)
-                        pv[t] = PLAIN ? rs * __uint_as_float(sc[t])
-                                      : fmaf(coef * load_alpha<AKH>(ak_t, t * p.G + g), __uint_as_float(sc[t]),
-                                             __uint_as_float(sr[t]));
+                        for (int t = 0; t < kT; ++t) pv[t] = rs * __uint_as_float(sc[t]);
+                    } else {
+                        // (coef alpha^k_t) S_c + S_r, two tokens per packed instruction
+                        const uint64_t coef2 = f2(coef, coef);
+#pragma unroll
+                        for (int t = 0; t < kT; t += 2) {
+                            const uint64_t ca = f2_mul(coef2, f2(load_alpha<AKH>(ak_t, t * p.G + g),
+                                                                 load_alpha<AKH>(ak_t, (t + 1) * p.G + g)));
+                            const float2 r2 = f2_unpack(f2_fma(ca, f2(__uint_as_float(sc[t]), __uint_as_float(sc[t + 1])),
+                                                               f2(__uint_as_float(sr[t]), __uint_as_float(sr[t + 1]))));
+                            pv[t] = r2.x;
+                            pv[t + 1] = r2.y;
+                        }
+                    }
                 }
                 if (valid < kT) {
 #pragma unroll
@@ -395,12 +406,14 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                                           fmaxf(fmaxf(mo[4], mo[5]), fmaxf(mo[6], mo[7])));
                 if (lane == 0) bulk_wait_read_all();
                 __syncwarp();
+                const uint64_t mo2 = f2(m_own, m_own);
 #pragma unroll
                 for (int c8 = 0; c8 < kT / 8; ++c8) {
                     uint32_t w[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const __half2 h2 = __floats2half2_rn(pv[8 * c8 + 2 * u] - m_own, pv[8 * c8 + 2 * u + 1] - m_own);
+                        const float2 d = f2_unpack(f2_sub(f2(pv[8 * c8 + 2 * u], pv[8 * c8 + 2 * u + 1]), mo2));
+                        const __half2 h2 = __floats2half2_rn(d.x, d.y);
                         w[u] = *reinterpret_cast<const uint32_t*>(&h2);
                     }
                     *reinterpret_cast<uint4*>(sY + xrow + ((c8 ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -484,6 +497,10 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 const bool fast = __all_sync(0xffffffffu, valid == kT && m_own + off <= m_run + 8.f);
                 float ps4[4] = {0.f, 0.f, 0.f, 0.f};
                 if (fast) {
+                    // two tokens per packed instruction: (lg + (off + x)) - m_run, then
+                    // two exponentials and the packed running sums
+                    const uint64_t off2 = f2(off, off), mr2 = f2(m_run, m_run);
+                    uint64_t ps2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t w16[16];
@@ -491,16 +508,18 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                         for (int q = 0; q < 16; ++q) {
                             const int t = 32 * h + 2 * q;
                             const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[t >> 1]));
-                            const float e0 = fast_exp2(lg[t] + (off + f.x) - m_run);
-                            const float e1 = fast_exp2(lg[t + 1] + (off + f.y) - m_run);
-                            ps4[q & 3] += e0 + e1;
+                            const float2 x2 = f2_unpack(f2_sub(f2_add(f2(lg[t], lg[t + 1]), f2_add(off2, f2(f.x, f.y))), mr2));
+                            const float e0 = fast_exp2(x2.x);
+                            const float e1 = fast_exp2(x2.y);
+                            ps2[q & 1] = f2_add(ps2[q & 1], f2(e0, e1));
                             const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
                             w16[q] = *reinterpret_cast<const uint32_t*>(&b2);
                         }
                         tmem_st16(tmem + kCP + pb * (kT / 2) + 16 * h + lane_base, w16);
                     }
                     tmem_wait_st();
-                    l_run += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+                    const float2 s0 = f2_unpack(ps2[0]), s1 = f2_unpack(ps2[1]);
+                    l_run += (s0.x + s0.y) + (s1.x + s1.y);
                 } else {
 #pragma unroll
                     for (int t = 0; t < kT; t += 2) {
