@@ -96,6 +96,12 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
+// Three-input maximum (one instruction on sm_100 and later); exact, like fmaxf.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 // Bounded wait: spins on try_wait, checks the wall clock every 256 polls and
 // gives up (recording QKMLA_ERR_TIMEOUT) after limit_ns.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, int* status,

@@ -405,8 +405,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
 #pragma unroll
                 for (int q = 0; q < kQ4; ++q)
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj)
-                        ca[q][jj] = coef * load_alpha<AKH>(ak_t, (32 * q + tb + jj) * p.G + g);
+                    for (int jj = 0; jj < 16; jj += 2) {      // two tokens per packed multiply
+                        const float2 c2 = f2_unpack(f2_mul(f2(coef, coef),
+                                                           f2(load_alpha<AKH>(ak_t, (32 * q + tb + jj) * p.G + g),
+                                                              load_alpha<AKH>(ak_t, (32 * q + tb + jj + 1) * p.G + g))));
+                        ca[q][jj] = c2.x;
+                        ca[q][jj + 1] = c2.y;
+                    }
             }
             uint32_t sc[kQ4][16], sr[kQ4][16];
 #pragma unroll
@@ -424,19 +429,29 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
             for (int q = 0; q < kQ4; ++q) {
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
-                    const int t = 32 * q + tb + jj;
-                    if (PLAIN)
+                    if (PLAIN) {
                         lg[q][jj] = rs * __uint_as_float(sc[q][jj]);
-                    else
-                        lg[q][jj] = fmaf(ca[q][jj], __uint_as_float(sc[q][jj]), __uint_as_float(sr[q][jj]));
-                    if (t >= valid_r) lg[q][jj] = -INFINITY;
+                    } else if ((jj & 1) == 0) {
+                        const float2 l2 = f2_unpack(f2_fma(f2(ca[q][jj], ca[q][jj + 1]),
+                                                           f2(__uint_as_float(sc[q][jj]), __uint_as_float(sc[q][jj + 1])),
+                                                           f2(__uint_as_float(sr[q][jj]), __uint_as_float(sr[q][jj + 1]))));
+                        lg[q][jj] = l2.x;
+                        lg[q][jj + 1] = l2.y;
+                    }
                 }
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    if (32 * q + tb + jj >= valid_r) lg[q][jj] = -INFINITY;
             }
             float mt = -INFINITY;
 #pragma unroll
-            for (int q = 0; q < kQ4; ++q)
+            for (int q = 0; q < kQ4; ++q) {
+                float m5[6];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) mt = fmaxf(mt, lg[q][jj]);
+                for (int i = 0; i < 5; ++i) m5[i] = fmax3(lg[q][3 * i], lg[q][3 * i + 1], lg[q][3 * i + 2]);
+                m5[5] = lg[q][15];
+                mt = fmax3(mt, fmax3(m5[0], m5[1], m5[2]), fmax3(m5[3], m5[4], m5[5]));
+            }
             mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
             // lazy running max: move it only when the tile max exceeds it by > 8 (log2)
             float corr = 1.f;
@@ -485,14 +500,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_consta
 #pragma unroll
             for (int q = 0; q < kQ4; ++q) {
                 uint32_t w8[8];
+                uint64_t ps2 = f2(0.f, 0.f);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const float e0 = fast_exp2(lg[q][2 * u] - m_e);
-                    const float e1 = fast_exp2(lg[q][2 * u + 1] - m_e);
-                    psum += e0 + e1;
+                    const float2 x2 = f2_unpack(f2_sub(f2(lg[q][2 * u], lg[q][2 * u + 1]), f2(m_e, m_e)));
+                    const float e0 = fast_exp2(x2.x);
+                    const float e1 = fast_exp2(x2.y);
+                    ps2 = f2_add(ps2, f2(e0, e1));
                     const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
                     w8[u] = *reinterpret_cast<const uint32_t*>(&b2);
                 }
+                const float2 s2 = f2_unpack(ps2);
+                psum += s2.x + s2.y;
                 if (row_ok) {
                     const int t = 32 * q + tb;
                     *reinterpret_cast<uint4*>(pT + pt_offset<KT>(r, t, rows_o)) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
