@@ -96,6 +96,15 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
     return d;
 }
 
+// c + (the two fp16 halves of w), each as one mixed-precision add (the half is
+// converted exactly, the sum rounded once: the same bits as converting first).
+__device__ __forceinline__ float2 half2_plus(uint32_t w, float c) {
+    float2 r;
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %3;\n\tadd.rn.f32.f16 %1, hi, %3;\n\t}"
+        : "=f"(r.x), "=f"(r.y) : "r"(w), "f"(c));
+    return r;
+}
 // Three-input maximum (one instruction on sm_100 and later); exact, like fmaxf.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;

@@ -499,7 +499,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 if (fast) {
                     // two tokens per packed instruction: (lg + (off + x)) - m_run, then
                     // two exponentials and the packed running sums
-                    const uint64_t off2 = f2(off, off), mr2 = f2(m_run, m_run);
+                    const uint64_t mr2 = f2(m_run, m_run);
                     uint64_t ps2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -507,8 +507,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
 #pragma unroll
                         for (int q = 0; q < 16; ++q) {
                             const int t = 32 * h + 2 * q;
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[t >> 1]));
-                            const float2 x2 = f2_unpack(f2_sub(f2_add(f2(lg[t], lg[t + 1]), f2_add(off2, f2(f.x, f.y))), mr2));
+                            const float2 a = half2_plus(xw[t >> 1], off);          // off + partner, exact as before
+                            const float2 x2 = f2_unpack(f2_sub(f2_add(f2(lg[t], lg[t + 1]), f2(a.x, a.y)), mr2));
                             const float e0 = fast_exp2(x2.x);
                             const float e1 = fast_exp2(x2.y);
                             ps2[q & 1] = f2_add(ps2[q & 1], f2(e0, e1));
@@ -523,9 +523,9 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 } else {
 #pragma unroll
                     for (int t = 0; t < kT; t += 2) {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[t >> 1]));
-                        lg[t] += off + f.x;
-                        lg[t + 1] += off + f.y;
+                        const float2 a = half2_plus(xw[t >> 1], off);
+                        lg[t] += a.x;
+                        lg[t + 1] += a.y;
                     }
                     if (valid < kT) {
 #pragma unroll
