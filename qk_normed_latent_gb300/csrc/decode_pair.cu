@@ -14,8 +14,10 @@
 // dimension: CTA r owns latent columns [256 r, 256 r + 256) and RoPE columns
 // [32 r, 32 r + 32).  Per 64-token tile each CTA
 //   * computes partial logits over its half of K (M=128 rows, N=64, K=288),
-//     and applies the alpha^q / alpha^k scaling to its content part (the
-//     scaling is linear, so partial logits add),
+//     and applies the column scaling alpha^k to its content part (the scaling
+//     is linear, so partial logits add); the row factor scale log2e alpha^q,
+//     common to both parts, is divided out of the RoPE query and applied once
+//     to the summed logit, in the exponent argument,
 //   * exchanges partials with the other CTA: every softmax warp stages its 32
 //     rows -- 64 fp16 values relative to the row's own maximum, plus that
 //     maximum in fp32, so the values near the maximum (the ones that matter
@@ -175,9 +177,11 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             float ss = 0.f;
 #pragma unroll
             for (int j = 0; j < kDR; ++j) ss = fmaf(v[j], v[j], ss);
-            // QK mode: scale*log2e rides on the RoPE query, so its MMA output is
-            // already the RoPE logit in the exp2 domain
-            const float beta = PLAIN ? 1.f : p.scale * kLog2e / sqrtf(ss / (float)kDR + p.eps);
+            // QK mode: the RoPE query carries 1 / (RMS alpha^q), so its MMA output is the
+            // RoPE logit in the exp2 domain divided by this row's content scale
+            // coef = scale log2e alpha^q: the softmax groups work in logit / coef units
+            // and apply coef once, in the exponent argument
+            const float beta = PLAIN ? 1.f : 1.f / (sqrtf(ss / (float)kDR + p.eps) * a);
             uint8_t* qrope = sQ + kQLat;
 #pragma unroll
             for (int j = 0; j < kHalfRope; j += 2) {
@@ -186,7 +190,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 const __nv_bfloat162 w2 = __floats2bfloat162_rn(v0 * gq[j] * beta, v1 * gq[j + 1] * beta);
                 *reinterpret_cast<__nv_bfloat162*>(qrope + sw64_offset(r, j)) = w2;
             }
-            coef_s[r] = PLAIN ? 0.f : p.scale * a * kLog2e;
+            coef_s[r] = PLAIN ? p.scale * kLog2e : p.scale * a * kLog2e;
         }
         fence_proxy_async_smem();
     }
@@ -342,8 +346,6 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
         float* const y_off = reinterpret_cast<float*>(sY + my_slice + 32 * kXRowB);
         if (grp_a) {
             const int g = (r % p.H) / hpg;
-            const float coef = coef_s[r];
-            const float rs = p.scale * kLog2e;
             const uint32_t peer_x = map_to_rank(smem_u32(sX) + my_slice, peer);
             const uint32_t peer_xfull = map_to_rank(smem_u32(&xfull[sub]), peer);
             float pv[kT];
@@ -365,15 +367,13 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                     if (lane == 0) mbar_arrive(sfree);
                     if (PLAIN) {
 #pragma unroll
-                        for (int t = 0; t < kT; ++t) pv[t] = rs * __uint_as_float(sc[t]);
+                        for (int t = 0; t < kT; ++t) pv[t] = __uint_as_float(sc[t]);
                     } else {
-                        // (coef alpha^k_t) S_c + S_r, two tokens per packed instruction
-                        const uint64_t coef2 = f2(coef, coef);
+                        // alpha^k_t S_c + S_r (logit / coef), two tokens per packed instruction
 #pragma unroll
                         for (int t = 0; t < kT; t += 2) {
-                            const uint64_t ca = f2_mul(coef2, f2(load_alpha<AKH>(ak_t, t * p.G + g),
-                                                                 load_alpha<AKH>(ak_t, (t + 1) * p.G + g)));
-                            const float2 r2 = f2_unpack(f2_fma(ca, f2(__uint_as_float(sc[t]), __uint_as_float(sc[t + 1])),
+                            const uint64_t ak2 = f2(load_alpha<AKH>(ak_t, t * p.G + g), load_alpha<AKH>(ak_t, (t + 1) * p.G + g));
+                            const float2 r2 = f2_unpack(f2_fma(ak2, f2(__uint_as_float(sc[t]), __uint_as_float(sc[t + 1])),
                                                                f2(__uint_as_float(sr[t]), __uint_as_float(sr[t + 1]))));
                             pv[t] = r2.x;
                             pv[t + 1] = r2.y;
@@ -439,6 +439,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
             __syncwarp();
         } else {
             const uint32_t peer_xfree = map_to_rank(smem_u32(&xfree[sub]), peer);
+            const float coef = coef_s[r];      // exp2-domain logit = coef x (this group's working units)
             // arm for tile 0's rows; the other CTA's copy may complete its bytes first
             // (the transaction count goes negative), the phase still needs this arrive
             if (lane == 0 && n_t > 0) mbar_arrive_expect_tx(&xfull[sub], kXSlice);
@@ -484,7 +485,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                     // overwrite these rows
                     uint32_t xdep = __float_as_uint(off);
 #pragma unroll
-                    for (int u = 0; u < kT / 2; ++u) xdep ^= xw[u];
+                    for (int u = 0; u < kT / 2; u += 4) xdep ^= xw[u];   // one word per 16-byte load
                     const uint32_t xdep_w = __reduce_xor_sync(0xffffffffu, xdep);
                     if (lane == 0 && j + 1 < n_t) {
                         mbar_arrive_expect_tx(&xfull[sub], kXSlice);
@@ -494,12 +495,12 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                 // own max + partner max bounds the tile max: when it cannot move the running
                 // max (by > 8, log2) for any row of the warp and the tile is full, the sums go
                 // straight into the exponentials
-                const bool fast = __all_sync(0xffffffffu, valid == kT && m_own + off <= m_run + 8.f);
+                const bool fast = __all_sync(0xffffffffu, valid == kT && coef * (m_own + off) <= m_run + 8.f);
                 float ps4[4] = {0.f, 0.f, 0.f, 0.f};
                 if (fast) {
                     // two tokens per packed instruction: (lg + (off + x)) - m_run, then
                     // two exponentials and the packed running sums
-                    const uint64_t mr2 = f2(m_run, m_run);
+                    const uint64_t c2 = f2(coef, coef), nm2 = f2(-m_run, -m_run);
                     uint64_t ps2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -508,7 +509,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                         for (int q = 0; q < 16; ++q) {
                             const int t = 32 * h + 2 * q;
                             const float2 a = half2_plus(xw[t >> 1], off);          // off + partner, exact as before
-                            const float2 x2 = f2_unpack(f2_sub(f2_add(f2(lg[t], lg[t + 1]), f2(a.x, a.y)), mr2));
+                            const float2 x2 = f2_unpack(f2_fma(c2, f2_add(f2(lg[t], lg[t + 1]), f2(a.x, a.y)), nm2));
                             const float e0 = fast_exp2(x2.x);
                             const float e1 = fast_exp2(x2.y);
                             ps2[q & 1] = f2_add(ps2[q & 1], f2(e0, e1));
@@ -534,14 +535,14 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                     }
                     float corr = 1.f;
                     bool need = false;
-                    if (m_own + off > m_run + 8.f) {
+                    if (coef * (m_own + off) > m_run + 8.f) {
                         float mx[8];                           // tree max: short dependency chains
 #pragma unroll
                         for (int q = 0; q < 8; ++q) mx[q] = fmaxf(fmaxf(lg[q], lg[q + 8]), fmaxf(lg[q + 16], lg[q + 24]));
 #pragma unroll
                         for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], fmaxf(fmaxf(lg[q + 32], lg[q + 40]), fmaxf(lg[q + 48], lg[q + 56])));
-                        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                        const float mt = coef * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
                         need = mt > m_run + 8.f;
                         if (need) {
                             corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mt);
@@ -572,8 +573,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_cons
                         uint32_t w16[16];
 #pragma unroll
                         for (int q = 0; q < 16; ++q) {
-                            const float e0 = fast_exp2(lg[32 * h + 2 * q] - m_run);
-                            const float e1 = fast_exp2(lg[32 * h + 2 * q + 1] - m_run);
+                            const float e0 = fast_exp2(fmaf(coef, lg[32 * h + 2 * q], -m_run));
+                            const float e1 = fast_exp2(fmaf(coef, lg[32 * h + 2 * q + 1], -m_run));
                             ps4[q & 3] += e0 + e1;
                             const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
                             w16[q] = *reinterpret_cast<const uint32_t*>(&b2);
