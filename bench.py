@@ -417,9 +417,13 @@ def main():
         sp_step_g, sp_dec_g = graphs_of(sp)
         sb_step_g, sb_dec_g = graphs_of(sb)
         kp = min(args.steps, 100)
-        p_step, p_dec = timed(sp_step_g, kp), timed(sp_dec_g, kp)
-        q_step, q_dec = timed(step_graph, kp), timed(dec_graph, kp)
-        b_step, b_dec = timed(sb_step_g, kp), timed(sb_dec_g, kp)
+        # the three variants' replays are interleaved one by one, so drift over the
+        # run (and the ~2 us modes of short replays) falls on all three alike
+        p_step, q_step, b_step, p_dec, q_dec, b_dec = [], [], [], [], [], []
+        for _ in range(kp):
+            for g_, out in ((sp_step_g, p_step), (step_graph, q_step), (sb_step_g, b_step),
+                            (sp_dec_g, p_dec), (dec_graph, q_dec), (sb_dec_g, b_dec)):
+                out += timed(g_, 1)
         med = statistics.median
         plain = {"decode_ms": med(p_dec), "qknorm_decode_ms": med(q_dec),
                  "overhead_pct": 100.0 * (med(q_dec) / med(p_dec) - 1.0),

@@ -6,7 +6,9 @@ a CTA overwriting the rows its partner is still reading.  Such a race shows as
 rare, small differences, which parity tolerances would hide; comparing bits
 over many calls exposes it.  The long-context workload (four 256k-token
 sequences, split over every CTA pair, thousands of tiles per pair) keeps the
-exchange running longest; the small one exercises the 64-row kernel."""
+exchange running longest; the small one exercises the 64-row kernel.  Whole
+steps (absorb, append, decode) are compared too, on the small workload and on
+the batch-128 one, whose absorb runs the persistent kernel."""
 import hashlib
 
 import pytest
@@ -45,3 +47,30 @@ def test_decode_repeats_bit_identical(Q, widx, repeats):
         h.update(st.lse.view(torch.uint8).cpu().numpy().tobytes())
         digests.append(h.hexdigest())
     assert len(set(digests)) == 1, f"{len(set(digests))} distinct outputs over {repeats} calls"
+
+
+def _digest(*tensors):
+    h = hashlib.sha1()
+    for t in tensors:
+        h.update(t.contiguous().view(torch.uint8).cpu().numpy().tobytes())
+    return h.hexdigest()
+
+
+@pytest.mark.parametrize("widx,repeats", [(1, 20), (4, 5)])
+def test_step_repeats_bit_identical(Q, widx, repeats):
+    """absorb -> append -> decode, repeated on the same inputs: q~, alpha^q, the
+    appended cache rows and alpha^k, o and lse all keep their bits."""
+    from qk_normed_latent_gb300.pipeline import DeviceState
+    st = DeviceState(W.WORKLOADS[widx], sentinel=False)
+    st.step()
+    torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    slots = st.slots_new.long()
+    digests = []
+    for k in range(repeats):
+        flush.fill_(k & 255)
+        st.step()
+        torch.cuda.synchronize()
+        assert Q.get_device_status() == 0
+        digests.append(_digest(st.q_tilde, st.alpha_q, st.kv[slots], st.ak[slots], st.o, st.lse))
+    assert len(set(digests)) == 1, f"{len(set(digests))} distinct step outputs over {repeats} steps"
