@@ -42,7 +42,7 @@ constexpr int kMaxJ = 8;       // d_h <= 256
 constexpr int kFT = 16;        // tokens per cluster
 constexpr int kKS = 64;        // d_c rows per CTA
 __host__ __device__ inline int split_smem_bytes(int d_h) {
-    return kFT * kKS * 4 + kKS * d_h * 4 + kFT * d_h * 4 + 16;
+    return kFT * kKS * 4 + kKS * d_h * 4 + kFT * d_h * 4 + 8 * kFT * 4 + 16;
 }
 
 // cluster-wide barrier (every thread of every CTA), DSMEM address of rank r, remote load
@@ -58,6 +58,9 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
+}
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // Latent (pure cast) and RoPE key (normalised on its own) of token n into slot s.
@@ -113,7 +116,8 @@ append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r
     float* Cs = reinterpret_cast<float*>(sm);                              // [kFT][kKS]
     float* Ws = Cs + kFT * kKS;                                            // [kKS][kDh]
     float* red = Ws + kKS * kDh;                                           // [kFT][kDh] partial keys
-    uint64_t* bar = reinterpret_cast<uint64_t*>(red + kFT * kDh);
+    float* ssp = red + kFT * kDh;                                          // [S][kFT] (CTA 0) sums of squares
+    uint64_t* bar = reinterpret_cast<uint64_t*>(ssp + 8 * kFT);
     const int tid = threadIdx.x;
     const int rank = (int)(blockIdx.x % S);
     const int g = blockIdx.y;
@@ -217,20 +221,33 @@ append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r
         }
     }
     cluster_sync_all();                    // every CTA's partial keys are in its shared memory
-    if (rank == 0) {
-        // k = sum over the cluster's CTAs in rank order, then the sum of squares
-        // over this thread's columns and across the 16 threads of the token
-        float ss = 0.f;
+    {
+        // The reduction is spread over the cluster: CTA r owns key columns
+        // [r kCpr, r kCpr + kCpr).  Each key element is the sum over the CTAs in rank
+        // order; this CTA's squares are added per token (thread (t, q): columns
+        // q + 16 i) and the token's sum of squares goes to CTA 0.
+        constexpr int kCpr = kDh / S;
+        float sq = 0.f;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t off = smem_u32(red + t * kDh + q + 16 * u);
-            float k = 0.f;
+        for (int i = 0; i < (kCpr + 15) / 16; ++i) {
+            const int cc = q + 16 * i;
+            if (cc < kCpr) {
+                const uint32_t off = smem_u32(red + t * kDh + rank * kCpr + cc);
+                float k = 0.f;
 #pragma unroll
-            for (int r = 0; r < S; ++r) k += ld_shared_cluster_f32(map_shared_rank(off, (uint32_t)r));
-            ss = fmaf(k, k, ss);
+                for (int r = 0; r < S; ++r) k += ld_shared_cluster_f32(map_shared_rank(off, (uint32_t)r));
+                sq = fmaf(k, k, sq);
+            }
         }
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        for (int o = 8; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        if (q == 0) st_shared_cluster_f32(map_shared_rank(smem_u32(ssp + rank * kFT + t), 0u), sq);
+    }
+    cluster_sync_all();                    // CTA 0 holds every CTA's sums; no CTA reads another's memory after this
+    if (rank == 0) {
+        float ss = 0.f;
+#pragma unroll
+        for (int r = 0; r < S; ++r) ss += ssp[r * kFT + t];
         if (q == 0 && tok && all_ok) {
             if (slot >= num_slots) {
                 report(status, QKMLA_ERR_DEVICE_BOUNDS);
@@ -269,7 +286,6 @@ append_split_kernel(const float* __restrict__ c_new, const float* __restrict__ r
             }
         }
     }
-    cluster_sync_all();                    // CTA 0 has read every CTA's partial keys
 }
 
 template <typename CT>
