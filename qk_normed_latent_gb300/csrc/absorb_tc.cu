@@ -372,9 +372,11 @@ absorb_tc_persistent(const __grid_constant__ CUtensorMap tm_out, const float* __
         // ---- this tile's q rows (the previous tile's output boxes have been read out) ----
         if (tid == 0) mbar_arrive_expect_tx(&bar[1], (uint32_t)(m_valid * DH * 4));
         __syncwarp();
-        if (tid < m_valid) {
-            const int m = m0 + tid, r = m / hpg, h = g * hpg + m % hpg;
-            bulk_load(rawA + tid * DH, q + ((size_t)r * H + h) * DH, DH * 4, &bar[1]);
+        // a query token's hpg heads of group g are contiguous (the launcher requires
+        // kM % hpg == 0, so a tile holds whole tokens): one copy per token
+        if (tid < m_valid / hpg) {
+            const int r = m0 / hpg + tid;
+            bulk_load(rawA + tid * hpg * DH, q + ((size_t)r * H + g * hpg) * DH, (uint32_t)(hpg * DH * 4), &bar[1]);
         }
         ok = mbar_wait(&bar[1], it & 1, 1u << 24);
         if (__syncthreads_or(!ok)) {
