@@ -237,7 +237,9 @@ size_t qkmla_decode_workspace_size(const qkmla_decode_args* a);
  * o[b][i][h] = sum_t p_t c_t with p = softmax_t(l); lse = log sum_t exp(l_t).
  * Long contexts are split over CTAs (split-KV) and merged by a combine kernel.
  * Errors: INVALID (null pointer, bad dims, H % G, d_c % 64 for bf16, ...),
- * UNSUPPORTED, WORKSPACE (workspace smaller than required).  Device-side:
+ * UNSUPPORTED (heads per group H / G other than 1, 2, 4, 8 or 16; d_c > 512
+ * or d_r > 128; a cache or output dtype other than fp32 / bf16), WORKSPACE
+ * (workspace smaller than required).  Device-side:
  * seq_len < s_q or > max_pages*page_size, or a page id outside
  * [0, num_slots/page_size), set QKMLA_ERR_DEVICE_BOUNDS; the sequence's
  * affected rows are then undefined.
