@@ -1002,7 +1002,9 @@ int launch_decode_tc(const qkmla_decode_args* a, const DecodePlan& plan, cudaStr
                    : launch_kernel<256, 32, false, 4, false>(lat, rope, qmap, tp, n_rb, max_items, s);
     }
     if (rc != QKMLA_OK) return rc;
-    const int combine_ctas = std::min(a->B * a->s_q * a->H, 2 * sms);
+    // one CTA per merged row where few sequences make few, long, split rows (every
+    // CTA computes the plan, so many CTAs cost more than they give on large batches)
+    const int combine_ctas = std::min(a->B * a->s_q * a->H, (a->B <= 32 ? 8 : 2) * sms);
     auto ck = a->d_c == 512 ? combine_var_kernel<4> : combine_var_kernel<2>;   // d_c = 128 x VEC
     return launch_pdl(ck, dim3(combine_ctas), dim3(128), 0, s, (const float*)o_part, (const float*)lse_part,
                       (const int*)seq_nsplit, (const int*)seq_part0, (const int*)split_list,
